@@ -1,0 +1,25 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA device (sm_103a) and the built library")
+    config.addinivalue_line(
+        "markers", "slow: full-size parity case (minutes of oracle time)")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The C-ABI library loaded through the thin binding (GPU tests only)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from flash_attention_gqa_gb300 import binding
+    return binding.load()
