@@ -1,0 +1,252 @@
+// C ABI of the GB300 blocked GQA flash-attention library: argument checks,
+// TMA tensor-map construction, kernel launches and the device status word.
+// Every check happens on the host before anything is enqueued; nothing here
+// allocates device memory or synchronises (except fa_check_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "kernels.h"
+
+namespace fa {
+// Device error word: bounded waits that give up OR their code in here.
+__device__ uint32_t g_fa_error = 0;
+}  // namespace fa
+
+namespace {
+
+using fa::kRows;
+
+std::atomic<uint64_t> g_wait_limit_ns{0};
+
+uint64_t wait_limit() {
+  uint64_t v = g_wait_limit_ns.load();
+  if (v == 0) {
+    v = 2000000000ull;
+    if (const char* e = std::getenv("FA_WAIT_LIMIT_NS")) {
+      const unsigned long long x = std::strtoull(e, nullptr, 10);
+      if (x > 0) v = x;
+    }
+    g_wait_limit_ns.store(v);
+  }
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Device address of the error word on the current device (cached per device).
+uint32_t* error_word() {
+  static uint32_t* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, fa::g_fa_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2_le128(int g) { return g >= 1 && g <= 128 && (g & (g - 1)) == 0; }
+
+// q-like tensor [B*K, G, T, H] as a 4-D map with a box of one Q tile x 64 dims.
+bool make_q_map(CUtensorMap* m, const void* ptr, int BK, int G, int T, int H) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)G, (cuuint64_t)BK};
+  cuuint64_t strides[3] = {(cuuint64_t)H * 2, (cuuint64_t)T * H * 2, (cuuint64_t)G * T * H * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)(kRows / G), (cuuint32_t)G, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// k-like tensor [B*K, S, H] as a 3-D map with a box of `rows` keys x 64 dims.
+bool make_kv_map(CUtensorMap* m, const void* ptr, int BK, int S, int H, int rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)BK};
+  cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)S * H * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared shape checks of the forward and backward passes.
+int check_shapes(int B, int K, int G, int T, int S, int H, int causal, const void* seg_q,
+                 const void* seg_kv) {
+  if (B < 0 || K < 0 || G < 0 || T < 0 || S < 0 || H < 0) return FA_ERR_INVALID_ARG;
+  if ((seg_q == nullptr) != (seg_kv == nullptr)) return FA_ERR_INVALID_ARG;
+  if (seg_q && (!aligned16(seg_q) || !aligned16(seg_kv))) return FA_ERR_INVALID_ARG;
+  if (H != 64 && H != 128 && H != 256) return FA_ERR_UNSUPPORTED;
+  if (!pow2_le128(G)) return FA_ERR_UNSUPPORTED;
+  if (T % kRows != 0 || S % fa::kKvRows != 0) return FA_ERR_UNSUPPORTED;
+  if (causal && T != S) return FA_ERR_UNSUPPORTED;
+  if (S / fa::kKvRows > fa::kMaxKvTiles) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * K > 65535) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
+           const int32_t* seg_kv, int causal, void* o, float* lse, int B, int K, int G, int T,
+           int S, int H, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long rows = (long)B * K * G * T;
+  if (rows == 0) return FA_OK;
+  if (S == 0) {
+    return fa::launch_fill_empty(o, lse, rows, H, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  fa::FwdArgs a{};
+  const int BK = B * K;
+  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
+      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows))
+    return FA_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.seg_q = seg_q;
+  a.seg_kv = seg_kv;
+  a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
+  a.causal = causal ? 1 : 0;
+  a.n_qtiles = T / (kRows / G);
+  a.err = error_word();
+  a.wait_limit_ns = wait_limit();
+  if (!a.err) return FA_ERR_CUDA;
+  return fa::launch_fwd(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {
+  (void)S; (void)H;
+  if (B <= 0 || K <= 0 || G <= 0 || T <= 0) return 0;
+  const size_t bytes = (size_t)B * K * G * T * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
+           void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
+           int S, int H, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
+  if (rc != FA_OK) return rc;
+  if (H == 64) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_bwd_workspace_size(B, K, G, T, S, H);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long rows = (long)B * K * G * T;
+  const int BK = B * K;
+  const int kvr = fa::bwd_kv_rows(H);
+  if (BK == 0) return FA_OK;
+  if (rows == 0 || S == 0) {
+    // No query rows or no keys: every gradient is zero.
+    if (rows > 0 && cudaMemsetAsync(dq, 0, (size_t)rows * H * 2, st) != cudaSuccess) return FA_ERR_CUDA;
+    if (S > 0 && (cudaMemsetAsync(dk, 0, (size_t)BK * S * H * 2, st) != cudaSuccess ||
+                  cudaMemsetAsync(dv, 0, (size_t)BK * S * H * 2, st) != cudaSuccess))
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  fa::BwdArgs a{};
+  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_q_map(&a.tm_do, dO, BK, G, T, H) ||
+      !make_kv_map(&a.tm_k, k, BK, S, H, kvr) || !make_kv_map(&a.tm_v, v, BK, S, H, kvr))
+    return FA_ERR_CUDA;
+  float* delta = static_cast<float*>(workspace);
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.seg_q = seg_q; a.seg_kv = seg_kv;
+  a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
+  a.causal = causal ? 1 : 0;
+  a.n_qtiles = T / (kRows / G);
+  a.n_kvtiles = S / kvr;
+  a.err = error_word();
+  a.wait_limit_ns = wait_limit();
+  if (!a.err) return FA_ERR_CUDA;
+  cudaError_t e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, st);
+  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(a, st);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq(a, st);
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_check_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t err = 0;
+  if (cudaMemcpyFromSymbol(&err, fa::g_fa_error, sizeof(err)) != cudaSuccess) return FA_ERR_CUDA;
+  if (err != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_error, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) return FA_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns);
+  return FA_OK;
+}
+
+int fa_selftest_wait_timeout(void* stream) {
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  if (fa::launch_wait_selftest(err, wait_limit(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa_check_status(stream);
+}
+
+int fa_device_sm_count(void) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,458 @@
+// Forward pass of blocked GQA flash attention on sm_103a.
+//
+// One CTA owns one Q tile: the G query heads of one kv head packed into 128
+// rows (row r = g * (128/G) + i, position t = t0 + i), loaded once by TMA.  It
+// sweeps the non-empty KV tiles of 128 keys with the online softmax of
+// "Chunked attention" (danielwatson6.github.io/fa/fa.html): running max m,
+// denominator l, accumulator O rescaled when m moves, O / l at the end; the
+// accumulator never leaves the chip and the T x S weights never reach memory
+// ("Optimizing the kernel": carries kept on chip, bf16 output).
+//
+// Roles (warp specialisation, 192 threads):
+//   warps 0-3  softmax: thread r owns TMEM lane r = packed row r
+//   warp  4    TMA producer (lane 0): Q once, then K/V in 16 KB chunks
+//   warp  5    MMA issuer (lane 0) and TMEM owner
+//
+// Tensor memory (512 columns): O accumulator in columns [0, H); two S buffers
+// of 128 fp32 columns at 256 and 384.  P (bf16, 2 per column) overwrites the
+// first 64 columns of its S buffer and is the A operand of O += P V.
+//
+// Shared memory: Q tile (H/64 chunks of [128 rows x 128 B]), a ring of
+// kSlots chunks of [128 keys x 64 dims] bf16 fed by TMA with 128-byte swizzle,
+// the per-tile schedule and the mbarriers.
+#include <cuda_bf16.h>
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSlots = 8;
+constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 128 B
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
+
+template <int H>
+struct FwdSmem {
+  static constexpr int HC = H / 64;
+  static constexpr uint32_t q_off = 0;
+  static constexpr uint32_t ring_off = HC * kChunkBytes;
+  static constexpr uint32_t tiles_off = ring_off + kSlots * kChunkBytes;   // uint16 schedule
+  static constexpr uint32_t cls_off = tiles_off + kMaxKvTiles * 2;         // uint8 classes
+  static constexpr uint32_t bar_off = cls_off + kMaxKvTiles;
+  // barriers: q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], pv_done[2], teardown
+  static constexpr int n_bars = 1 + 2 * kSlots + 7;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, count, qrange
+  static constexpr uint32_t bytes = misc_off + 64;
+  static constexpr uint32_t alloc = bytes + 1024;  // room to align the base to 1024
+};
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t empty(int s) const { return base + 8 * (1 + kSlots + s); }
+  __device__ uint32_t s_full(int b) const { return base + 8 * (1 + 2 * kSlots + b); }
+  __device__ uint32_t p_full(int b) const { return base + 8 * (3 + 2 * kSlots + b); }
+  __device__ uint32_t pv_done(int b) const { return base + 8 * (5 + 2 * kSlots + b); }
+  __device__ uint32_t teardown() const { return base + 8 * (7 + 2 * kSlots); }
+};
+
+// All lanes of a warp agree on the outcome of a bounded wait, so the
+// warp-collective TMEM accesses that follow are executed by all or none.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  const bool ok = mbar_wait(bar, parity, ab);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Tile classes of the lazy mask.
+enum : uint8_t { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
+
+template <int H>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using L = FwdSmem<H>;
+  constexpr int HC = L::HC;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(sm);
+
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(sm + L::tiles_off);
+  uint8_t* cls = sm + L::cls_off;
+  Bars bars{sbase + L::bar_off};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc_off + 4);
+  int* n_tiles_s = reinterpret_cast<int*>(sm + L::misc_off + 8);
+  int* qrange = reinterpret_cast<int*>(sm + L::misc_off + 16);
+  const Abort ab{abort_flag, a.wait_limit_ns, a.err};
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int Tb = kRows / a.G;                      // positions per Q tile
+  const int qt = a.n_qtiles - 1 - (int)blockIdx.x;  // heaviest (latest) tiles first
+  const int bk = blockIdx.y;
+  const int b = bk / a.K;
+  const int t0 = qt * Tb;
+  const int n_kv_all = a.S / kKvRows;
+  const bool segs = a.seg_q != nullptr;
+
+  // ---------------------------------------------------------------- setup
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bars.q_full(), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full(i), 1);
+      mbar_init(bars.p_full(i), kRows);
+      mbar_init(bars.pv_done(i), 1);
+    }
+    mbar_init(bars.teardown(), 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 4) {
+    prefetch_tmap(&a.tm_q);
+    prefetch_tmap(&a.tm_k);
+    prefetch_tmap(&a.tm_v);
+  }
+
+  // KV tiles the causal mask can reach: keys s <= t_max.
+  int n_kv = n_kv_all;
+  if (a.causal) n_kv = min(n_kv_all, (t0 + Tb - 1) / kKvRows + 1);
+
+  // Segment range of this Q tile (ids of its Tb positions).
+  if (segs && warp == 0) {
+    int mn = INT_MAX, mx = INT_MIN;
+    for (int i = lane; i < Tb; i += 32) {
+      int v = a.seg_q[(long)b * a.T + t0 + i];
+      mn = min(mn, v);
+      mx = max(mx, v);
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) { qrange[0] = mn; qrange[1] = mx; }
+  }
+  __syncthreads();
+
+  // Classify every reachable KV tile (lazy mask: only per-tile id ranges).
+  for (int j = warp; j < n_kv; j += kThreads / 32) {
+    uint8_t c = TILE_FULL;
+    if (a.causal && (j + 1) * kKvRows - 1 > t0) c = TILE_PARTIAL;  // crosses the diagonal
+    if (segs) {
+      const int4 v = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + j * kKvRows)[lane];
+      int mn = min(min(v.x, v.y), min(v.z, v.w));
+      int mx = max(max(v.x, v.y), max(v.z, v.w));
+      mn = __reduce_min_sync(0xffffffffu, mn);
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      const int qmn = qrange[0], qmx = qrange[1];
+      if (mx < qmn || mn > qmx) c = TILE_EMPTY;
+      else if (!(mn == mx && qmn == qmx && mn == qmn)) c = TILE_PARTIAL;
+    }
+    if (lane == 0) cls[j] = c;
+  }
+  __syncthreads();
+  // Compact the non-empty tiles into the schedule (warp 0, ballot prefix sums).
+  if (warp == 0) {
+    int count = 0;
+    for (int j0 = 0; j0 < n_kv; j0 += 32) {
+      const int j = j0 + lane;
+      const uint8_t c = j < n_kv ? cls[j] : TILE_EMPTY;
+      const uint32_t m = __ballot_sync(0xffffffffu, c != TILE_EMPTY);
+      if (c != TILE_EMPTY) {
+        const int pos = count + __popc(m & ((1u << lane) - 1));
+        tiles[pos] = (uint16_t)(j | (c == TILE_PARTIAL ? 0x8000 : 0));
+      }
+      count += __popc(m);
+    }
+    if (lane == 0) *n_tiles_s = count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_tiles = *n_tiles_s;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_tiles > 0) {
+      mbar_arrive_expect_tx(bars.q_full(), HC * kChunkBytes);
+      for (int c = 0; c < HC; ++c)
+        tma_load_4d(sbase + L::q_off + c * kChunkBytes, &a.tm_q, bars.q_full(), c * 64, t0, 0, bk);
+      uint32_t seq = 0;
+      bool ok = true;
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        const int j = tiles[n] & 0x7fff;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const CUtensorMap* m = kv == 0 ? &a.tm_k : &a.tm_v;
+          for (int c = 0; c < HC; ++c, ++seq) {
+            const int slot = seq % kSlots;
+            if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
+            tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
+                        j * kKvRows, bk);
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA exits.
+        const uint32_t first = seq > kSlots ? seq - kSlots : 0;
+        for (uint32_t s = first; s < seq; ++s)
+          mbar_wait_teardown(bars.full(s % kSlots), (s / kSlots) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
+      constexpr uint32_t id_o = idesc_bf16(128, 64, false, true);    // O[:, 64c:] += P V_c
+      bool ok = mbar_wait(bars.q_full(), 0, ab);
+      auto issue_pv = [&](int n) -> bool {
+        if (!mbar_wait(bars.p_full(n & 1), (n >> 1) & 1, ab)) return false;
+        tc_fence_after();
+        const uint32_t p_col = 256 + 128 * (n & 1);
+        for (int c = 0; c < HC; ++c) {
+          const uint32_t seq = (uint32_t)n * 2 * HC + HC + c;
+          const int slot = seq % kSlots;
+          if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) return false;
+          tc_fence_after();
+          const uint32_t vbase = sbase + L::ring_off + slot * kChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < kKvRows / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, kChunkBytes, 1024);
+            mma_ts(tmem + c * 64, tmem + p_col + kk * 8, bdesc, id_o, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bars.empty(slot));
+        }
+        mma_commit(bars.pv_done(n & 1));
+        return true;
+      };
+      for (int n = 0; n < n_tiles && ok; ++n) {
+        // S buffer n&1 (and the P inside it) is free once O += P V of tile n-2 is done.
+        if (n >= 2 && !mbar_wait(bars.pv_done(n & 1), ((n - 2) >> 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t s_col = 256 + 128 * (n & 1);
+        for (int c = 0; c < HC && ok; ++c) {
+          const uint32_t seq = (uint32_t)n * 2 * HC + c;
+          const int slot = seq % kSlots;
+          if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qc = sbase + L::q_off + c * kChunkBytes;
+          const uint32_t kc = sbase + L::ring_off + slot * kChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_ss(tmem + s_col, sdesc_sw128(qc + kk * 32, 16, 1024),
+                   sdesc_sw128(kc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bars.empty(slot));
+        }
+        if (!ok) break;
+        mma_commit(bars.s_full(n & 1));
+        if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
+      }
+      if (ok) ok = issue_pv(n_tiles - 1);
+      if (!ok) {
+        // Wait (bounded) for every MMA this thread issued before TMEM is freed.
+        mma_commit(bars.teardown());
+        mbar_wait_teardown(bars.teardown(), 0, a.wait_limit_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = tid;  // TMEM lane == packed row
+    const int g = r / Tb;
+    const int t = t0 + (r - g * Tb);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int my_seg = segs ? a.seg_q[(long)b * a.T + t] : 0;
+    float m_ref = -INFINITY;  // running max, log2 units
+    float l = 0.f;            // running denominator (relative to m_ref)
+    bool ok = true;
+    for (int n = 0; n < n_tiles; ++n) {
+      const int j = tiles[n] & 0x7fff;
+      const bool partial = (tiles[n] & 0x8000) != 0;
+      if (!warp_wait(bars.s_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t s_col = 256 + 128 * (n & 1);
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + s_col + c * 32, sv[c]);
+      tmem_wait_ld();
+      float* s = reinterpret_cast<float*>(&sv[0][0]);
+      if (partial) {
+        const int s0 = j * kKvRows;
+        if (a.causal) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (s0 + c > t) s[c] = -INFINITY;
+        }
+        if (segs) {
+          // every thread reads the same 512 B of key ids: served by L1 broadcast
+          const int4* kid = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + s0);
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 v = __ldg(kid + c4);
+            if (v.x != my_seg) s[4 * c4 + 0] = -INFINITY;
+            if (v.y != my_seg) s[4 * c4 + 1] = -INFINITY;
+            if (v.z != my_seg) s[4 * c4 + 2] = -INFINITY;
+            if (v.w != my_seg) s[4 * c4 + 3] = -INFINITY;
+          }
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * kLog2e;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (n == 0) {
+        m_ref = m_tile;
+      } else if (m_tile > m_ref + kRescaleThreshold) {
+        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_tile);
+        m_ref = m_tile;
+        rescale = true;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = fast_exp2(fmaf(s[2 * c], kLog2e, -m_use));
+        const float p1 = fast_exp2(fmaf(s[2 * c + 1], kLog2e, -m_use));
+        sum += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      // O must be rescaled before O += P V of this tile; it holds every earlier tile.
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!warp_wait(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < H; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tmem + lane_base + c, ov);
+        }
+      }
+      tmem_st32(tmem + lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tmem + lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bars.p_full(n & 1));
+    }
+    // ------------------------------------------------------------ epilogue
+    const long row = ((long)bk * a.G + g) * a.T + t;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + row * H;
+    const bool have = n_tiles > 0 && ok &&
+                      warp_wait(bars.pv_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, ab);
+    if (have) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < H; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_base + c, ov);
+        tmem_wait_ld();
+        uint4 pkd[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+      }
+      a.lse[row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    } else {
+      uint4 z = make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < H; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+      a.lse[row] = -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void fill_empty_kernel(__nv_bfloat16* o, float* lse, long rows, int H) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < rows * H) o[i] = __float2bfloat16(0.f);
+  if (i < rows) lse[i] = -INFINITY;
+}
+
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const Abort ab{&flag, limit_ns, err};
+  // Nothing ever arrives on this barrier: the bounded wait must give up.
+  mbar_wait(smem_u32(&bar), 0, ab);
+  __syncthreads();
+}
+
+template <int H>
+cudaError_t launch_fwd_h(const FwdArgs& a, cudaStream_t st) {
+  using L = FwdSmem<H>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<H>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  dim3 grid(a.n_qtiles, a.B * a.K);
+  fa_fwd_kernel<H><<<grid, kThreads, L::alloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
+  switch (a.H) {
+    case 64: return launch_fwd_h<64>(a, st);
+    case 128: return launch_fwd_h<128>(a, st);
+    case 256: return launch_fwd_h<256>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fill_empty(void* o, float* lse, long rows, int H, cudaStream_t st) {
+  const long n = rows * (long)H > rows ? rows * (long)H : rows;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const long blocks = (n + threads - 1) / threads;
+  fill_empty_kernel<<<(unsigned)blocks, threads, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(o), lse,
+                                                          rows, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

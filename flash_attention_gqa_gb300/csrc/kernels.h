@@ -1,0 +1,60 @@
+// Internal interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Tile geometry shared by every kernel.
+constexpr int kRows = 128;     // packed query rows per Q tile (G heads x 128/G positions)
+constexpr int kKvRows = 128;   // key/value rows per KV tile in the forward
+constexpr int kMaxKvTiles = 1024;  // S <= 131072
+
+struct FwdArgs {
+  CUtensorMap tm_q;   // q as 4-D {H, T, G, B*K}, box {64, 128/G, G, 1}, 128B swizzle
+  CUtensorMap tm_k;   // k as 3-D {H, S, B*K},   box {64, 128, 1}
+  CUtensorMap tm_v;   // v, same as k
+  void* o;            // bf16 [B*K, G, T, H]
+  float* lse;         // [B*K, G, T]
+  const int32_t* seg_q;   // [B, T] or null
+  const int32_t* seg_kv;  // [B, S] or null
+  int B, K, G, T, S, H;
+  int causal;
+  int n_qtiles;       // T / (128 / G)
+  uint32_t* err;      // device error word
+  uint64_t wait_limit_ns;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q;    // q  as 4-D, box {64, 128/G, G, 1}
+  CUtensorMap tm_do;   // dO as 4-D, same box
+  CUtensorMap tm_k;    // k as 3-D, box {64, kv_rows, 1}
+  CUtensorMap tm_v;    // v as 3-D, box {64, kv_rows, 1}
+  const float* lse;    // [B*K, G, T]
+  const float* delta;  // [B*K, G, T]  D = rowsum(dO * o)
+  void* dq;            // bf16 [B*K, G, T, H]
+  void* dk;            // bf16 [B*K, S, H]
+  void* dv;            // bf16 [B*K, S, H]
+  const int32_t* seg_q;
+  const int32_t* seg_kv;
+  int B, K, G, T, S, H;
+  int causal;
+  int n_qtiles;        // T / (128 / G)
+  int n_kvtiles;       // S / kv_rows
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
+                                  cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_fill_empty(void* o, float* lse, long rows, int H, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
+
+// KV rows per tile of the backward kernels for a head dim.
+constexpr int bwd_kv_rows(int H) { return H == 256 ? 64 : 128; }
+
+}  // namespace fa

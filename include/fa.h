@@ -1,0 +1,120 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) blocked GQA flash-attention library
+ * (libfa_gb300.so).  Plain pointers and sizes only; no framework types.
+ *
+ * Notation ("Notation", danielwatson6.github.io/fa/fa.html):
+ *   B batch, K kv heads, G query heads per kv head, T queries, S keys, H head dim.
+ *
+ * Layouts (all tensors dense, row-major in the order given, innermost last):
+ *   q, o, dO, dq : [B, K, G, T, H]  bf16 (IEEE bfloat16 stored as uint16)
+ *   k, v, dk, dv : [B, K, S, H]     bf16
+ *   lse          : [B, K, G, T]     float32, natural-log logsumexp of the rows
+ *   seg_q        : [B, T] int32,   seg_kv : [B, S] int32 (both or neither)
+ * q arrives already multiplied by H**-0.5; the library applies no scale of its
+ * own ("What is wrong with naive attention?": queries pre-scaled by H^-1/2).
+ *
+ * Ownership: the caller owns every buffer (device memory, 16-byte aligned, as
+ * TMA requires) including the backward workspace.  The library allocates no
+ * device memory, never synchronises, and enqueues all work on `stream`
+ * (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *
+ * Errors: every call validates all arguments on the host before launching
+ * anything and returns one of the FA_* codes below.  A bounded device-side
+ * wait that runs out of time sets a device error word; fa_check_status()
+ * reports it as FA_ERR_DEVICE_TIMEOUT (and clears it).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, one seg pointer without the
+                                 other, misaligned pointer, workspace too small */
+  FA_ERR_UNSUPPORTED = 2,     /* H not in {64,128,256}, G not a power of two <= 128,
+                                 T or S not a multiple of 128, causal with T != S,
+                                 backward with H == 64 */
+  FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device wait ran out (kernel gave up) */
+};
+
+/*
+ * Forward pass: for every (b, k, g, t)
+ *   o[b,k,g,t,:]  = sum_s softmax_s(L)[s] * v[b,k,s,:],  L[s] = q[b,k,g,t,:] . k[b,k,s,:]
+ *   lse[b,k,g,t]  = log sum_s exp(L[s])
+ * over the keys kept by the mask: s <= t when `causal` (same absolute index for
+ * queries and keys), and seg_q[b,t] == seg_kv[b,s] when segment ids are given
+ * (SegmentIds, jax_flash_attn_tpu docs: only tokens with the same id attend).
+ * This is the online-softmax sweep of "Chunked attention" / "Optimizing the
+ * kernel" (running max m, denominator, rescaled accumulator, output divided
+ * by the denominator at the end; bf16 output from an fp32 accumulator).
+ * Rows with no kept key get o = 0 and lse = -inf.  The T x S weights are never
+ * written to memory and no mask array exists: masks are generated per tile
+ * and tiles the mask removes entirely are skipped (axlearn PR "Optimize TPU
+ * Flash Attention", lazy causal mask).
+ * T == 0 or S == 0 or B*K == 0: no kernel work beyond filling o = 0, lse = -inf.
+ */
+int fa_fwd(const void* q, const void* k, const void* v,
+           const int32_t* seg_q, const int32_t* seg_kv, int causal,
+           void* o, float* lse,
+           int B, int K, int G, int T, int S, int H, void* stream);
+
+/* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256). */
+size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
+
+/*
+ * Backward pass for the loss sum(o * dO): writes dq, dk, dv (bf16).
+ *   P  = exp(L - lse)            (recomputed per tile from the saved lse)
+ *   dP = dO . v^T,  dS = P * (dP - D),  D[b,k,g,t] = sum_h dO * o
+ *   dq = dS . k,  dk = sum_g dS^T . q,  dv = sum_g P^T . dO
+ * The pages give no backward; this is the textbook derivative of the forward
+ * definition above.  `o` and `lse` must be those fa_fwd produced for the same
+ * inputs.  `workspace` (>= fa_bwd_workspace_size bytes, 256-byte aligned)
+ * holds the fp32 D rows; its contents on entry do not matter.
+ * Supported head dims: 128 and 256.
+ */
+int fa_bwd(const void* q, const void* k, const void* v,
+           const void* o, const float* lse, const void* dO,
+           const int32_t* seg_q, const int32_t* seg_kv, int causal,
+           void* dq, void* dk, void* dv,
+           void* workspace, size_t workspace_bytes,
+           int B, int K, int G, int T, int S, int H, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_CUDA.
+ */
+int fa_check_status(void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fa_status_string(int status);
+
+/*
+ * Time limit, in nanoseconds, of every bounded device wait launched after
+ * this call (default 2e9, or the FA_WAIT_LIMIT_NS environment variable).
+ * Returns FA_ERR_INVALID_ARG for 0.
+ */
+int fa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier no one arrives on, with the current limit, and returns the status
+ * fa_check_status() reports afterwards (FA_ERR_DEVICE_TIMEOUT when the
+ * machinery works).  Faults nothing and leaves the context usable.
+ */
+int fa_selftest_wait_timeout(void* stream);
+
+/* Number of SMs of the current device (0 on error); used for grid sizing. */
+int fa_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

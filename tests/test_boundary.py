@@ -1,0 +1,87 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+include/fa.h declares, and host-side validation rejects bad arguments before
+anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from flash_attention_gqa_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    if not os.path.exists(binding.LIB_PATH):
+        from flash_attention_gqa_gb300 import build
+        build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(clib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(clib, n), n
+        assert n in binding.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings(clib):
+    for code in range(5):
+        assert binding.status_string(code)
+    assert binding.status_string(99) == "unknown status"
+
+
+def test_workspace_size(clib):
+    assert binding.fa_bwd_workspace_size(1, 2, 8, 8192, 8192, 256) == 2 * 8 * 8192 * 4
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 1, 128, 128) == 256
+    assert binding.fa_bwd_workspace_size(0, 1, 1, 128, 128, 128) == 0
+
+
+def _fwd(clib, *, q=16, k=16, v=16, sq=None, skv=None, causal=0, o=16, lse=16,
+         B=1, K=1, G=4, T=128, S=128, H=128):
+    P = ctypes.c_void_p
+    return clib.fa_fwd(P(q), P(k), P(v), P(sq), P(skv), causal, P(o), P(lse),
+                       B, K, G, T, S, H, None)
+
+
+def test_fwd_validation(clib):
+    assert _fwd(clib, q=0) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(clib, q=8) == binding.FA_ERR_INVALID_ARG            # misaligned
+    assert _fwd(clib, sq=16) == binding.FA_ERR_INVALID_ARG           # one seg pointer
+    assert _fwd(clib, B=-1) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(clib, H=96) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, G=3) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, G=256) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, T=100, S=100) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, causal=1, T=128, S=256) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, S=256 * 1024) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(clib, T=0) == binding.FA_OK                          # nothing to do
+
+
+def test_bwd_validation(clib):
+    P = ctypes.c_void_p
+
+    def call(ws=256, ws_bytes=1 << 20, H=128, dq=16):
+        return clib.fa_bwd(P(16), P(16), P(16), P(16), P(16), P(16), None, None, 1,
+                           P(dq), P(16), P(16), P(ws), ws_bytes, 1, 1, 4, 128, 128, H, None)
+
+    assert call(dq=0) == binding.FA_ERR_INVALID_ARG
+    assert call(ws=0) == binding.FA_ERR_INVALID_ARG
+    assert call(ws=272) == binding.FA_ERR_INVALID_ARG                 # not 256-aligned
+    assert call(ws_bytes=16) == binding.FA_ERR_INVALID_ARG
+    assert call(H=64) == binding.FA_ERR_UNSUPPORTED
+
+
+def test_wait_limit_setter(clib):
+    assert binding.fa_set_wait_limit_ns(0) == binding.FA_ERR_INVALID_ARG
+    assert binding.fa_set_wait_limit_ns(2_000_000_000) == binding.FA_OK
