@@ -118,13 +118,16 @@ extern "C" {
 int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
            const int32_t* seg_kv, int causal, void* o, float* lse, int B, int K, int G, int T,
            int S, int H, void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Pointers are required (and must be aligned) only for tensors with elements.
   const long rows = (long)B * K * G * T;
+  const bool has_kv = (long)B * K * S > 0;
+  if (rows > 0 && (!q || !o || !lse || !aligned16(q) || !aligned16(o) ||
+                   (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return FA_ERR_INVALID_ARG;
+  if (has_kv && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows == 0) return FA_OK;
   if (S == 0) {
     return fa::launch_fill_empty(o, lse, rows, H, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -148,22 +151,26 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
 }
 
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {
-  (void)S; (void)H;
-  if (B <= 0 || K <= 0 || G <= 0 || T <= 0) return 0;
-  const size_t bytes = (size_t)B * K * G * T * sizeof(float);
-  return (bytes + 255) & ~(size_t)255;
+  if (B <= 0 || K <= 0 || G <= 0 || T <= 0 || S < 0) return 0;
+  if (check_shapes(B, K, G, T, S, H, 0, nullptr, nullptr) != FA_OK) return 0;
+  return fa::bwd_workspace_bytes(B, K, G, T, S, H);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
            void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
            int S, int H, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
-    return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
+  // Pointers are required (and must be aligned) only for tensors with elements.
+  const bool has_rows = (long)B * K * G * T > 0;
+  const bool has_kv = (long)B * K * S > 0;
+  if (has_rows && (!q || !o || !lse || !dO || !dq || !aligned16(q) || !aligned16(o) ||
+                   !aligned16(dO) || !aligned16(dq) || !aligned16(lse)))
+    return FA_ERR_INVALID_ARG;
+  if (has_kv && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
+                 !aligned16(dv)))
+    return FA_ERR_INVALID_ARG;
   if (H == 64) return FA_ERR_UNSUPPORTED;
   const size_t need = fa_bwd_workspace_size(B, K, G, T, S, H);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
@@ -199,6 +206,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
   cudaError_t e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, st);
+  if (e == cudaSuccess) e = fa::launch_seg_ranges(a, st);
   if (e == cudaSuccess) e = fa::launch_bwd_dkdv(a, st);
   if (e == cudaSuccess) e = fa::launch_bwd_dq(a, st);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;

@@ -1,11 +1,552 @@
-// Backward pass of blocked GQA flash attention on sm_103a (placeholder until
-// the tcgen05 kernels land): the D preprocess only.
+// Backward pass of blocked GQA flash attention on sm_103a.
+//
+// The pages give no backward; this is the derivative of the forward written
+// out (P = exp(L - lse), dP = dO V^T, dS = P (dP - D), dq = dS K,
+// dk = sum_g dS^T q, dv = sum_g P^T dO) in four launches:
+//   1. preprocess   D[row] = sum_h dO * o (fp32), one warp per row
+//   2. seg ranges   per-tile [min, max] segment ids (only with SegmentIds)
+//   3. dK/dV        one CTA per (kv tile, b*K): K and V stay in shared memory,
+//                   the non-empty Q tiles (G heads packed, 128 rows) stream by;
+//                   S = Q K^T and dP = dO V^T recomputed in TMEM, P and dS
+//                   written to shared memory, and dV^T += dO^T P,
+//                   dK^T += Q^T dS accumulated in TMEM with the head dim on the
+//                   128 lanes (so H = 256 fits in tensor memory).
+//   4. dQ           one CTA per (Q tile, b*K): Q and dO stay in shared memory,
+//                   the non-empty KV tiles stream by; dS goes to TMEM as the A
+//                   operand of dQ += dS K.
+// The two gradient passes recompute S and dP (7 tile products instead of 5)
+// and in exchange need no atomics: every output element is written once by
+// one CTA, so the result is deterministic.
 #include <cuda_bf16.h>
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace fa {
 namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kQChunk = 128 * 128;  // [128 rows x 64 dims] bf16
+constexpr float kLog2e = 1.4426950408889634f;
+enum : int { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Abort& ab) {
+  const bool ok = mbar_wait(bar, parity, ab);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Mask class of the (Q tile, KV tile) pair; q tile covers positions
+// [t0, t0 + Tb), kv tile [s0, s0 + kvr).  Segment ranges come from the
+// per-tile [min, max] table (conservative for non-monotone ids).
+__device__ __forceinline__ int tile_class(const BwdArgs& a, const int2* qr, const int2* kr, int b,
+                                          int qt, int jt, int Tb, int kvr) {
+  const int t0 = qt * Tb, s0 = jt * kvr;
+  int c = TILE_FULL;
+  if (a.causal) {
+    if (t0 + Tb - 1 < s0) return TILE_EMPTY;
+    if (t0 < s0 + kvr - 1) c = TILE_PARTIAL;
+  }
+  if (a.seg_q != nullptr) {
+    const int2 q = qr[(long)b * a.n_qtiles + qt];
+    const int2 k = kr[(long)b * a.n_kvtiles + jt];
+    if (k.y < q.x || k.x > q.y) return TILE_EMPTY;
+    if (!(q.x == q.y && k.x == k.y && q.x == k.x)) c = TILE_PARTIAL;
+  }
+  return c;
+}
+
+// Apply the causal / segment mask to 32 consecutive key columns of one row.
+__device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int t, int my_seg,
+                                       int scol) {
+  if (a.causal) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (scol + i > t) s[i] = -INFINITY;
+  }
+  if (a.seg_q != nullptr) {
+    const int4* kid = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + scol);
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+      const int4 v = __ldg(kid + i4);
+      if (v.x != my_seg) s[4 * i4 + 0] = -INFINITY;
+      if (v.y != my_seg) s[4 * i4 + 1] = -INFINITY;
+      if (v.z != my_seg) s[4 * i4 + 2] = -INFINITY;
+      if (v.w != my_seg) s[4 * i4 + 3] = -INFINITY;
+    }
+  }
+}
+
+// =================================================================== dQ
+template <int H>
+struct DqCfg {
+  static constexpr int BN = bwd_kv_rows(H);            // keys per KV tile
+  static constexpr int HC = H / 64;
+  static constexpr int NBUF = (H + 4 * BN <= 512) ? 2 : 1;  // S/dP TMEM buffers
+  static constexpr uint32_t KV_CHUNK = BN * 128;       // [BN rows x 64 dims]
+  // K chunks live from S(n) to dQ(n) (two tiles in flight); V chunks from
+  // dP(n) only.  Separate rings keep the two lifetimes from blocking each other.
+  static constexpr int KSL = 2 * HC;
+  static constexpr int VSL = H == 256 ? HC : 2 * HC;
+  static constexpr uint32_t q_off = 0;
+  static constexpr uint32_t do_off = HC * kQChunk;
+  static constexpr uint32_t k_off = 2 * HC * kQChunk;
+  static constexpr uint32_t v_off = k_off + KSL * KV_CHUNK;
+  static constexpr uint32_t bar_off = v_off + VSL * KV_CHUNK;
+  // q_full, kfull[KSL], kempty[KSL], vfull[VSL], vempty[VSL], sdp_full[2], ds_full[2], dq_done[2], teardown
+  static constexpr int n_bars = 1 + 2 * KSL + 2 * VSL + 7;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;
+  static constexpr uint32_t alloc = misc_off + 64 + 1024;
+  __host__ __device__ static constexpr uint32_t s_col(int u) { return H + u * 2 * BN; }
+  __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + u * 2 * BN + BN; }
+};
+
+template <int H>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+  using C = DqCfg<H>;
+  constexpr int HC = C::HC, BN = C::BN, NBUF = C::NBUF, KSL = C::KSL, VSL = C::VSL;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + C::bar_off;
+  auto q_full = [&] { return bar0; };
+  auto kfull = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto kempty = [&](int s) { return bar0 + 8 * (1 + KSL + s); };
+  auto vfull = [&](int s) { return bar0 + 8 * (1 + 2 * KSL + s); };
+  auto vempty = [&](int s) { return bar0 + 8 * (1 + 2 * KSL + VSL + s); };
+  constexpr int xb = 1 + 2 * KSL + 2 * VSL;
+  auto sdp_full = [&](int u) { return bar0 + 8 * (xb + u); };
+  auto ds_full = [&](int u) { return bar0 + 8 * (xb + 2 + u); };
+  auto dq_done = [&](int u) { return bar0 + 8 * (xb + 4 + u); };
+  const uint32_t teardown = bar0 + 8 * (xb + 6);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
+  const Abort ab{abort_flag, a.wait_limit_ns, a.err};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Tb = kRows / a.G;
+  const int qt = a.n_qtiles - 1 - (int)blockIdx.x;
+  const int bk = blockIdx.y, b = bk / a.K;
+  const int t0 = qt * Tb;
+  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* kr = qr + (long)a.B * a.n_qtiles;
+  // qr/kr are only read when segment ids are given (they live past D).
+  int jt_end = a.n_kvtiles;
+  if (a.causal) jt_end = min(a.n_kvtiles, (t0 + Tb - 1) / BN + 1);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(q_full(), 1);
+    for (int s = 0; s < KSL; ++s) { mbar_init(kfull(s), 1); mbar_init(kempty(s), 1); }
+    for (int s = 0; s < VSL; ++s) { mbar_init(vfull(s), 1); mbar_init(vempty(s), 1); }
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(sdp_full(u), 1);
+      mbar_init(ds_full(u), kRows);
+      mbar_init(dq_done(u), 1);
+    }
+    mbar_init(teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t seq = 0;  // chunk sequence number, per ring (same for K and V)
+      uint32_t k_issued = 0, v_issued = 0;
+      bool any = false;
+      for (int jt = 0; jt < jt_end && ok; ++jt) {
+        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (!any) {
+          any = true;
+          mbar_arrive_expect_tx(q_full(), 2 * HC * kQChunk);
+          for (int c = 0; c < HC; ++c) {
+            tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(), c * 64, t0, 0, bk);
+            tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, q_full(), c * 64, t0, 0, bk);
+          }
+        }
+        for (int c = 0; c < HC && ok; ++c) {
+          const uint32_t sq = seq + c;
+          const int slot = sq % KSL;
+          if (sq >= KSL && !mbar_wait(kempty(slot), ((sq / KSL) - 1) & 1, ab)) { ok = false; break; }
+          mbar_arrive_expect_tx(kfull(slot), C::KV_CHUNK);
+          tma_load_3d(sbase + C::k_off + slot * C::KV_CHUNK, &a.tm_k, kfull(slot), c * 64, jt * BN, bk);
+          ++k_issued;
+        }
+        for (int c = 0; c < HC && ok; ++c) {
+          const uint32_t sq = seq + c;
+          const int slot = sq % VSL;
+          if (sq >= VSL && !mbar_wait(vempty(slot), ((sq / VSL) - 1) & 1, ab)) { ok = false; break; }
+          mbar_arrive_expect_tx(vfull(slot), C::KV_CHUNK);
+          tma_load_3d(sbase + C::v_off + slot * C::KV_CHUNK, &a.tm_v, vfull(slot), c * 64, jt * BN, bk);
+          ++v_issued;
+        }
+        seq += HC;
+      }
+      if (!ok) {
+        // Let copies in flight land before the CTA exits (bounded waits).
+        for (uint32_t sq = k_issued > KSL ? k_issued - KSL : 0; sq < k_issued; ++sq)
+          mbar_wait_teardown(kfull(sq % KSL), (sq / KSL) & 1, a.wait_limit_ns);
+        for (uint32_t sq = v_issued > VSL ? v_issued - VSL : 0; sq < v_issued; ++sq)
+          mbar_wait_teardown(vfull(sq % VSL), (sq / VSL) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);
+      constexpr uint32_t id_q = idesc_bf16(128, 64, false, true);
+      bool ok = true, waited_q = false;
+      int n = 0;
+      // Issue dQ(m) += dS(m) K(m) for the m-th processed tile.
+      auto issue_dq = [&](int m) -> bool {
+        const int u = m % NBUF;
+        if (!mbar_wait(ds_full(u), (m / NBUF) & 1, ab)) return false;
+        tc_fence_after();
+        for (int c = 0; c < HC; ++c) {
+          const uint32_t sq = (uint32_t)m * HC + c;
+          const int slot = sq % KSL;
+          const uint32_t kb = sbase + C::k_off + slot * C::KV_CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + c * 64, tmem + C::s_col(u) + kk * 8, sdesc_sw128(kb + kk * 2048, C::KV_CHUNK, 1024),
+                   id_q, (m > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(kempty(slot));
+        }
+        mma_commit(dq_done(u));
+        return true;
+      };
+      for (int jt = 0; jt < jt_end && ok; ++jt) {
+        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (!waited_q) {
+          if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
+          waited_q = true;
+        }
+        const int u = n % NBUF;
+        if (n >= NBUF && !mbar_wait(dq_done(u), ((n / NBUF) - 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        for (int c = 0; c < HC && ok; ++c) {  // S = Q K^T
+          const uint32_t sq = (uint32_t)n * HC + c;
+          const int slot = sq % KSL;
+          if (!mbar_wait(kfull(slot), (sq / KSL) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qc = sbase + C::q_off + c * kQChunk;
+          const uint32_t kc = sbase + C::k_off + slot * C::KV_CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::s_col(u), sdesc_sw128(qc + kk * 32, 16, 1024),
+                   sdesc_sw128(kc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        for (int c = 0; c < HC && ok; ++c) {  // dP = dO V^T
+          const uint32_t sq = (uint32_t)n * HC + c;
+          const int slot = sq % VSL;
+          if (!mbar_wait(vfull(slot), (sq / VSL) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t dc = sbase + C::do_off + c * kQChunk;
+          const uint32_t vc = sbase + C::v_off + slot * C::KV_CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::dp_col(u), sdesc_sw128(dc + kk * 32, 16, 1024),
+                   sdesc_sw128(vc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(vempty(slot));
+        }
+        if (!ok) break;
+        mma_commit(sdp_full(u));
+        if (n >= NBUF - 1 && !issue_dq(n - (NBUF - 1))) { ok = false; break; }
+        ++n;
+      }
+      for (int m = n - (NBUF - 1); ok && m < n; ++m)
+        if (m >= 0 && !issue_dq(m)) ok = false;
+      if (!ok) {
+        mma_commit(teardown);
+        mbar_wait_teardown(teardown, 0, a.wait_limit_ns);
+      }
+    }
+  } else {
+    // softmax-side: thread r owns packed query row r
+    const int r = tid, g = r / Tb, t = t0 + (r - g * Tb);
+    const long row = ((long)bk * a.G + g) * a.T + t;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float lse = a.lse[row];
+    const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+    const float Dr = a.delta[row];
+    const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
+    bool ok = true;
+    int n = 0;
+    for (int jt = 0; jt < jt_end; ++jt) {
+      const int cls = tile_class(a, qr, kr, b, qt, jt, Tb, BN);
+      if (cls == TILE_EMPTY) continue;
+      const int u = n % NBUF;
+      if (!warp_wait(sdp_full(u), (n / NBUF) & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tmem + lane_base + C::s_col(u) + c * 32, sv);
+        tmem_ld32(tmem + lane_base + C::dp_col(u) + c * 32, pv);
+        tmem_wait_ld();
+        float* s = reinterpret_cast<float*>(sv);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, t, my_seg, jt * BN + c * 32);
+        uint32_t ds[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(fmaf(s[2 * i], kLog2e, -lse2));
+          const float p1 = fast_exp2(fmaf(s[2 * i + 1], kLog2e, -lse2));
+          const float d0 = p0 * (__uint_as_float(pv[2 * i]) - Dr);
+          const float d1 = p1 * (__uint_as_float(pv[2 * i + 1]) - Dr);
+          ds[i] = pack_bf16x2(d0, d1);
+        }
+        // dS (bf16, 2 per column) overwrites S columns already read.
+        tmem_st16(tmem + lane_base + C::s_col(u) + c * 16, ds);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full(u));
+      ++n;
+    }
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + row * H;
+    const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) % NBUF), ((n - 1) / NBUF) & 1, ab);
+    if (have) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < H; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + c, v);
+        tmem_wait_ld();
+        uint4 pk[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst + c)[i] = pk[i];
+      }
+    } else {
+      for (int c = 0; c < H; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+// ================================================================ dK/dV
+template <int H>
+struct DkvCfg {
+  static constexpr int BN = bwd_kv_rows(H);   // keys per CTA
+  static constexpr int HC = H / 64;
+  static constexpr int HH = H / 128;          // 128-lane halves of the head dim
+  static constexpr int PC = BN / 64;          // 64-key chunks of P / dS
+  static constexpr uint32_t KV_CHUNK = BN * 128;
+  static constexpr uint32_t k_off = 0;
+  static constexpr uint32_t v_off = HC * KV_CHUNK;
+  static constexpr uint32_t q_off = 2 * HC * KV_CHUNK;
+  static constexpr uint32_t do_off = q_off + HC * kQChunk;
+  static constexpr uint32_t p_off = do_off + HC * kQChunk;
+  static constexpr uint32_t ds_off = p_off + PC * kQChunk;
+  static constexpr uint32_t bar_off = ds_off + PC * kQChunk;
+  // kv_full, q_full, q_empty, sdp_full, ps_full, teardown
+  static constexpr uint32_t misc_off = bar_off + 6 * 8;
+  static constexpr uint32_t alloc = misc_off + 64 + 1024;
+  static constexpr uint32_t dv_col = 0;
+  static constexpr uint32_t dk_col = HH * BN;
+  static constexpr uint32_t s_col = 2 * HH * BN;
+  static constexpr uint32_t dp_col = 2 * HH * BN + BN;
+};
+
+template <int H>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  using C = DkvCfg<H>;
+  constexpr int HC = C::HC, HH = C::HH, BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + C::bar_off;
+  const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = bar0 + 16, sdp_full = bar0 + 24,
+                 ps_full = bar0 + 32, teardown = bar0 + 40;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
+  const Abort ab{abort_flag, a.wait_limit_ns, a.err};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Tb = kRows / a.G;
+  const int jt = blockIdx.x;  // kv tile; early (causally heaviest) tiles first
+  const int bk = blockIdx.y, b = bk / a.K;
+  const int s0 = jt * BN;
+  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* kr = qr + (long)a.B * a.n_qtiles;
+  const int qt_begin = a.causal ? s0 / Tb : 0;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(kv_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(sdp_full, 1);
+    mbar_init(ps_full, kRows);
+    mbar_init(teardown, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      bool ok = true, any = false;
+      int i = 0;
+      for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
+        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (!any) {
+          any = true;
+          mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
+          for (int c = 0; c < HC; ++c) {
+            tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
+            tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
+          }
+        }
+        if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
+        mbar_arrive_expect_tx(q_full, 2 * HC * kQChunk);
+        for (int c = 0; c < HC; ++c) {
+          tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full, c * 64, qt * Tb, 0, bk);
+          tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, q_full, c * 64, qt * Tb, 0, bk);
+        }
+        ++i;
+      }
+      if (!ok && i > 0) mbar_wait_teardown(q_full, (i - 1) & 1, a.wait_limit_ns);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);  // S, dP: [128 q x BN]
+      constexpr uint32_t id_t = idesc_bf16(128, BN, true, true);    // dV^T, dK^T: [128 h x BN]
+      bool ok = true;
+      int i = 0;
+      for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
+        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
+        if (!mbar_wait(q_full, i & 1, ab)) { ok = false; break; }
+        // S / dP TMEM is free once the softmax side has read the previous tile.
+        if (i > 0 && !mbar_wait(ps_full, (i - 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        for (int c = 0; c < HC; ++c) {
+          const uint32_t qc = sbase + C::q_off + c * kQChunk, kc = sbase + C::k_off + c * C::KV_CHUNK;
+          const uint32_t dc = sbase + C::do_off + c * kQChunk, vc = sbase + C::v_off + c * C::KV_CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_ss(tmem + C::s_col, sdesc_sw128(qc + kk * 32, 16, 1024), sdesc_sw128(kc + kk * 32, 16, 1024),
+                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + C::dp_col, sdesc_sw128(dc + kk * 32, 16, 1024), sdesc_sw128(vc + kk * 32, 16, 1024),
+                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(sdp_full);
+        if (!mbar_wait(ps_full, i & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        for (int h = 0; h < HH; ++h) {
+          const uint32_t dA = sbase + C::do_off + 2 * h * kQChunk;
+          const uint32_t qA = sbase + C::q_off + 2 * h * kQChunk;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // contraction over the 128 packed query rows
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            mma_ss(tmem + C::dv_col + h * BN, sdesc_sw128(dA + kk * 2048, kQChunk, 1024),
+                   sdesc_sw128(sbase + C::p_off + kk * 2048, kQChunk, 1024), id_t, acc);
+            mma_ss(tmem + C::dk_col + h * BN, sdesc_sw128(qA + kk * 2048, kQChunk, 1024),
+                   sdesc_sw128(sbase + C::ds_off + kk * 2048, kQChunk, 1024), id_t, acc);
+          }
+        }
+        mma_commit(q_empty);
+        ++i;
+      }
+      if (!ok) {
+        mma_commit(teardown);
+        mbar_wait_teardown(teardown, 0, a.wait_limit_ns);
+      }
+    }
+  } else {
+    const int r = tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    int i = 0;
+    for (int qt = qt_begin; qt < a.n_qtiles; ++qt) {
+      const int cls = tile_class(a, qr, kr, b, qt, jt, Tb, BN);
+      if (cls == TILE_EMPTY) continue;
+      const int g = r / Tb, t = qt * Tb + (r - g * Tb);
+      const long row = ((long)bk * a.G + g) * a.T + t;
+      const float lse = a.lse[row];
+      const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+      const float Dr = a.delta[row];
+      const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
+      if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
+      // P / dS shared buffers are free once the previous tile's dV, dK products are done.
+      if (i > 0 && !warp_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
+        tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
+        tmem_wait_ld();
+        float* s = reinterpret_cast<float*>(sv);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, t, my_seg, s0 + c * 32);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = fast_exp2(fmaf(s[2 * k], kLog2e, -lse2));
+          const float p1 = fast_exp2(fmaf(s[2 * k + 1], kLog2e, -lse2));
+          pp[k] = pack_bf16x2(p0, p1);
+          dd[k] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * k]) - Dr), p1 * (__uint_as_float(pv[2 * k + 1]) - Dr));
+        }
+        // Row r of the [128 q x 64 key] chunk, 128-byte swizzle: 16-byte unit u
+        // of the row lands at unit u ^ (r % 8).
+        const int chunk = (c * 32) / 64;
+        const int u0 = ((c * 32) % 64) / 8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t off = chunk * kQChunk + r * 128 + (((u0 + k) ^ (r & 7)) * 16);
+          *reinterpret_cast<uint4*>(sm + C::p_off + off) = *reinterpret_cast<uint4*>(&pp[4 * k]);
+          *reinterpret_cast<uint4*>(sm + C::ds_off + off) = *reinterpret_cast<uint4*>(&dd[4 * k]);
+        }
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor cores
+      tc_fence_before();
+      mbar_arrive(ps_full);
+      ++i;
+    }
+    // Epilogue: lanes carry the head dim, columns the keys.
+    const bool have = i > 0 && ok && warp_wait(q_empty, (i - 1) & 1, ab);
+    if (have) tc_fence_after();
+    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
+    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
+#pragma unroll 1
+    for (int h = 0; h < HH; ++h) {
+      const int hd = h * 128 + r;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t vv[32], kv[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + C::dv_col + h * BN + c, vv);
+          tmem_ld32(tmem + lane_base + C::dk_col + h * BN + c, kv);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
+          dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
 
 // D[row] = sum_h dO[row, h] * o[row, h] in fp32; one warp per row.
 __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
@@ -18,15 +559,15 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
   const uint4* pd = reinterpret_cast<const uint4*>(dO + row * H);
   float acc = 0.f;
   for (int i = lane; i < H / 8; i += 32) {
-    const uint4 a = __ldg(po + i), d = __ldg(pd + i);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const uint4 x = __ldg(po + i), d = __ldg(pd + i);
+    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&x);
     const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 fa2 = __bfloat1622float2(a2[j]);
-      const float2 fd2 = __bfloat1622float2(d2[j]);
-      acc = fmaf(fa2.x, fd2.x, acc);
-      acc = fmaf(fa2.y, fd2.y, acc);
+      const float2 fx = __bfloat1622float2(x2[j]);
+      const float2 fd = __bfloat1622float2(d2[j]);
+      acc = fmaf(fx.x, fd.x, acc);
+      acc = fmaf(fx.y, fd.y, acc);
     }
   }
 #pragma unroll
@@ -34,7 +575,62 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
   if (lane == 0) delta[row] = acc;
 }
 
+// Per-tile [min, max] of segment ids: one warp per (b, tile).
+__global__ void seg_ranges_kernel(const int32_t* __restrict__ seg, int L, int tile, int n_tiles,
+                                  long total, int2* __restrict__ out) {
+  const long w = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= total) return;
+  const long b = w / n_tiles;
+  const int j = (int)(w - b * n_tiles);
+  const int32_t* p = seg + b * L + (long)j * tile;
+  int mn = INT_MAX, mx = INT_MIN;
+  for (int i = lane; i < tile; i += 32) {
+    const int v = __ldg(p + i);
+    mn = min(mn, v);
+    mx = max(mx, v);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) out[w] = make_int2(mn, mx);
+}
+
+template <typename Kern>
+cudaError_t set_smem(Kern k, uint32_t bytes, int* configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (*configured == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *configured = dev;
+  return e;
+}
+
+template <int H>
+cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st) {
+  static int configured = -1;
+  cudaError_t e = set_smem(fa_bwd_dq_kernel<H>, DqCfg<H>::alloc, &configured);
+  if (e != cudaSuccess) return e;
+  fa_bwd_dq_kernel<H><<<dim3(a.n_qtiles, a.B * a.K), kThreads, DqCfg<H>::alloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int H>
+cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
+  static int configured = -1;
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H>, DkvCfg<H>::alloc, &configured);
+  if (e != cudaSuccess) return e;
+  fa_bwd_dkdv_kernel<H><<<dim3(a.n_kvtiles, a.B * a.K), kThreads, DkvCfg<H>::alloc, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
+  const size_t d = ((size_t)B * K * G * T * sizeof(float) + 255) & ~(size_t)255;
+  const size_t nq = (size_t)T / (kRows / G), nk = (size_t)S / bwd_kv_rows(H);
+  const size_t r = ((size_t)B * (nq + nk) * sizeof(int2) + 255) & ~(size_t)255;
+  return d + r;
+}
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
                                   cudaStream_t st) {
@@ -46,7 +642,34 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, l
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dkdv(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd_dq(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
+  if (a.seg_q == nullptr) return cudaSuccess;
+  int2* qr = reinterpret_cast<int2*>(const_cast<float*>(a.delta) + (long)a.B * a.K * a.G * a.T);
+  int2* kr = qr + (long)a.B * a.n_qtiles;
+  const int Tb = kRows / a.G;
+  const long nq = (long)a.B * a.n_qtiles, nk = (long)a.B * a.n_kvtiles;
+  const int warps = 8;
+  seg_ranges_kernel<<<(unsigned)((nq + warps - 1) / warps), warps * 32, 0, st>>>(a.seg_q, a.T, Tb,
+                                                                                a.n_qtiles, nq, qr);
+  seg_ranges_kernel<<<(unsigned)((nk + warps - 1) / warps), warps * 32, 0, st>>>(
+      a.seg_kv, a.S, bwd_kv_rows(a.H), a.n_kvtiles, nk, kr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
+  switch (a.H) {
+    case 128: return launch_dkdv_h<128>(a, st);
+    case 256: return launch_dkdv_h<256>(a, st);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st) {
+  switch (a.H) {
+    case 128: return launch_dq_h<128>(a, st);
+    case 256: return launch_dq_h<256>(a, st);
+    default: return cudaErrorNotSupported;
+  }
+}
 
 }  // namespace fa

@@ -49,6 +49,7 @@ struct BwdArgs {
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
                                   cudaStream_t st);
+cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_fill_empty(void* o, float* lse, long rows, int H, cudaStream_t st);
@@ -56,5 +57,8 @@ cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t 
 
 // KV rows per tile of the backward kernels for a head dim.
 constexpr int bwd_kv_rows(int H) { return H == 256 ? 64 : 128; }
+
+// Backward workspace: fp32 D rows, then per-tile segment-id ranges.
+size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H);
 
 }  // namespace fa

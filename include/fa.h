@@ -65,7 +65,8 @@ int fa_fwd(const void* q, const void* k, const void* v,
            void* o, float* lse,
            int B, int K, int G, int T, int S, int H, void* stream);
 
-/* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256). */
+/* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256;
+   0 for empty or unsupported sizes). */
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
 
 /*
@@ -76,7 +77,8 @@ size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
  * The pages give no backward; this is the textbook derivative of the forward
  * definition above.  `o` and `lse` must be those fa_fwd produced for the same
  * inputs.  `workspace` (>= fa_bwd_workspace_size bytes, 256-byte aligned)
- * holds the fp32 D rows; its contents on entry do not matter.
+ * holds the fp32 D rows and per-tile segment-id ranges; its contents on
+ * entry do not matter.
  * Supported head dims: 128 and 256.
  */
 int fa_bwd(const void* q, const void* k, const void* v,

@@ -42,9 +42,13 @@ def test_status_strings(clib):
 
 
 def test_workspace_size(clib):
-    assert binding.fa_bwd_workspace_size(1, 2, 8, 8192, 8192, 256) == 2 * 8 * 8192 * 4
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 1, 128, 128) == 256
+    # fp32 D rows, then one (min, max) int32 pair per (b, q tile) and (b, kv tile)
+    n = binding.fa_bwd_workspace_size(1, 2, 8, 8192, 8192, 256)
+    assert n == 2 * 8 * 8192 * 4 + (8192 // 16 + 8192 // 64) * 8
+    assert n % 256 == 0
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256
     assert binding.fa_bwd_workspace_size(0, 1, 1, 128, 128, 128) == 0
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 128) == 0   # unsupported
 
 
 def _fwd(clib, *, q=16, k=16, v=16, sq=None, skv=None, causal=0, o=16, lse=16,

@@ -1,0 +1,101 @@
+"""Backward parity: fa_fwd + fa_bwd (through the C ABI) against the fp64
+oracle's analytic gradients on the same seeded bf16 inputs.  GPU only."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flash_attention_gqa_gb300 import binding, inputs
+from _parity import check_grad, check_lse, check_o, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(B, K, G, T, S, H, causal=False, seg_q=None, seg_kv=None, seed=0):
+    x = inputs.make_tensors(B, K, G, T, S, H, seed=seed, backward=True, seg_q=seg_q,
+                            seg_kv=seg_kv)
+    dev = torch.device("cuda")
+    q, k, v, dO = (t.to(dev) for t in (x.q, x.k, x.v, x.dO))
+    sq = None if x.seg_q is None else x.seg_q.to(dev)
+    skv = None if x.seg_kv is None else x.seg_kv.to(dev)
+    o, lse = binding.attention_forward(q, k, v, causal=causal, seg_q=sq, seg_kv=skv)
+    dq, dk, dv = binding.attention_backward(q, k, v, o, lse, dO, causal=causal, seg_q=sq,
+                                            seg_kv=skv)
+    assert binding.fa_check_status() == binding.FA_OK
+    kw = dict(causal=causal, seg_q=x.seg_q, seg_kv=x.seg_kv)
+    o_ref, l_ref = oracle.attention_forward(x.q, x.k, x.v, **kw)
+    g_ref = oracle.attention_backward(x.q, x.k, x.v, x.dO, **kw)
+    check_o(to_np(o), o_ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), l_ref)
+    errs = {}
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), g_ref):
+        errs[name] = check_grad(to_np(g), r, name)
+    return (dq, dk, dv), g_ref, errs
+
+
+@pytest.mark.parametrize("H", [128, 256])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_shapes(H, G, causal):
+    run_case(1, 2, G, 384, 384, H, causal=causal, seed=100 + H + G)
+
+
+@pytest.mark.parametrize("G", [16, 64])
+def test_wide_groups(G):
+    run_case(1, 1, G, 256, 256, 128, causal=True, seed=G)
+
+
+def test_rectangular_noncausal():
+    run_case(2, 1, 4, 128, 640, 128, causal=False, seed=13)
+    run_case(1, 2, 2, 512, 128, 256, causal=False, seed=14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H", [128, 256])
+def test_random_nonmonotone_segments(causal, H):
+    B, T = 2, 512
+    seg = inputs.random_segment_ids(B, T, 3, seed=17)
+    run_case(B, 2, 4, T, T, H, causal=causal, seg_q=seg, seg_kv=seg, seed=15)
+
+
+def test_document_segments_causal():
+    B, T = 3, 1024
+    seg = inputs.document_segment_ids(B, T, seed=0, lo=50, hi=400)
+    run_case(B, 2, 4, T, T, 128, causal=True, seg_q=seg, seg_kv=seg, seed=16)
+
+
+def test_fully_masked_rows_get_zero_gradient():
+    B, T = 1, 256
+    seg_q = np.zeros((B, T), dtype=np.int32)
+    seg_kv = np.zeros((B, T), dtype=np.int32)
+    seg_q[0, 100:140] = 7
+    (dq, _, _), _, _ = run_case(B, 1, 4, T, T, 128, causal=False, seg_q=seg_q,
+                                seg_kv=seg_kv, seed=18)
+    assert torch.all(dq[0, 0, :, 100:140] == 0)
+
+
+def test_causal_workload_h128_t1024_full():
+    w = inputs.WORKLOADS["gqa_causal_h128_t1024"]
+    run_case(w.B, w.K, w.G, w.T, w.S, w.H, causal=True, seed=w.seed)
+
+
+def test_backward_is_deterministic():
+    x = inputs.make_tensors(1, 2, 8, 512, 512, 256, seed=19, backward=True)
+    dev = torch.device("cuda")
+    q, k, v, dO = (t.to(dev) for t in (x.q, x.k, x.v, x.dO))
+    o, lse = binding.attention_forward(q, k, v, causal=True)
+    a = binding.attention_backward(q, k, v, o, lse, dO, causal=True)
+    b = binding.attention_backward(q, k, v, o, lse, dO, causal=True)
+    for x1, x2 in zip(a, b):
+        assert torch.equal(x1, x2)
+
+
+def test_h64_backward_is_rejected():
+    dev = torch.device("cuda")
+    q = torch.zeros(1, 1, 4, 128, 64, device=dev, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 128, 64, device=dev, dtype=torch.bfloat16)
+    o, lse = binding.attention_forward(q, k, k)
+    rc = binding.fa_bwd(q, k, k, o, lse, q, None, None, False, torch.empty_like(q),
+                        torch.empty_like(k), torch.empty_like(k),
+                        torch.empty(4096, device=dev, dtype=torch.uint8), check=False)
+    assert rc == binding.FA_ERR_UNSUPPORTED
