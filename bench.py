@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the blocked GQA flash-attention hot path (forward + backward).
+
+One step = fa_fwd + fa_bwd (every kernel of the path) over one batch of the
+seeded synthetic workload, inputs already resident in HBM.  Prints ONE JSON
+line (rank 0).  Metric: attention fwd+bwd TFLOP/s, mask-adjusted, i.e.
+4*B*K*G*H*(kept query/key pairs) for the forward and 2.5x that for the
+backward, over the device time of the step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle, same metric
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (the
+(batch, kv head) units are independent, so there is no data exchange); the
+only collectives are the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from flash_attention_gqa_gb300 import inputs
+
+METRIC = "attention fwd+bwd TFLOP/s (mask-adjusted) on 1 GB300; % of bf16 dense peak"
+DEFAULT_WORKLOAD = "gqa_causal_h256_t8192"
+L2_BYTES = 129 * 2**20
+
+# DRAM traffic per launch of the roofline kernel from one ncu capture, keyed
+# by kernel name; valid only while the kernel source hashes to `src_sha`.
+NCU_TRAFFIC = {
+    # profiles/kernels_gqa_causal_h256_t8192.md (ncu --set full, one launch each)
+    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 174813952, "src_sha": "929d0165f0a9896f"},
+    "fa_bwd_dq_kernel": {"bytes_per_launch": 188100608, "src_sha": "929d0165f0a9896f"},
+    "fa_fwd_kernel": {"bytes_per_launch": 107298304, "src_sha": "86eb98f27f267b2b"},
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=2048,
+                   help="query positions in the oracle's timed sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------- bookkeeping
+
+def flop_counts(w: inputs.Workload, seg: np.ndarray | None):
+    pairs = inputs.unmasked_pairs(w.T, w.S, w.causal, seg, seg, B=w.B)
+    fwd = 4.0 * w.K * w.G * w.H * pairs
+    return fwd, (2.5 * fwd if w.backward else 0.0), pairs / (w.B * w.T * w.S)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def src_sha(name: str) -> str:
+    with open(os.path.join(ROOT, "flash_attention_gqa_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- oracle
+
+def oracle_sample(w: inputs.Workload, x: inputs.Tensors, rows: int):
+    """The first `rows` query positions of the workload (with the keys they can
+    see when causal) as a self-contained sub-problem for the CPU oracle."""
+    rows = min(rows, w.T)
+    sl = lambda t, ax, n: t.narrow(ax, 0, n)
+    nkeys = rows if w.causal else w.S
+    sub = dict(q=sl(x.q, 3, rows), k=sl(x.k, 2, nkeys), v=sl(x.v, 2, nkeys),
+               dO=None if x.dO is None else sl(x.dO, 3, rows),
+               seg_q=None if x.seg_q is None else sl(x.seg_q, 1, rows),
+               seg_kv=None if x.seg_kv is None else sl(x.seg_kv, 1, nkeys))
+    segq = None if sub["seg_q"] is None else sub["seg_q"].numpy()
+    segk = None if sub["seg_kv"] is None else sub["seg_kv"].numpy()
+    pairs = inputs.unmasked_pairs(rows, nkeys, w.causal, segq, segk, B=w.B)
+    fwd = 4.0 * w.K * w.G * w.H * pairs
+    flop = fwd * (3.5 if w.backward else 1.0)
+    desc = (f"first {rows} of {w.T} query positions x all {w.B * w.K * w.G} heads "
+            f"against {'the keys they can see' if w.causal else 'all keys'}; "
+            f"{'forward + backward' if w.backward else 'forward'}")
+    return sub, flop, desc
+
+
+def run_oracle_step(w, sub):
+    import oracle  # the CPU oracle: only the baseline / reference legs use it
+    kw = dict(causal=w.causal, seg_q=sub["seg_q"], seg_kv=sub["seg_kv"])
+    oracle.attention_forward(sub["q"], sub["k"], sub["v"], **kw)
+    if w.backward:
+        oracle.attention_backward(sub["q"], sub["k"], sub["v"], sub["dO"], **kw)
+
+
+def cpu_baseline(w, x, rows):
+    sub, flop, desc = oracle_sample(w, x, rows)
+    t = time.perf_counter()
+    run_oracle_step(w, sub)
+    dt = time.perf_counter() - t
+    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": desc + f"; numpy fp64, BLAS pool of {os.cpu_count()} threads"}
+
+
+# ------------------------------------------------------------------ arms
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a per-rank timing over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    return world, rank, local
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make_workload(w)
+    # Size the sample so the whole run stays within about two and a half
+    # minutes: time a 256-row sample once (untimed) and scale by the causal
+    # (quadratic) or linear growth of the work with the number of rows.
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    probe, _, _ = oracle_sample(w, x, 256)
+    t = time.perf_counter()
+    run_oracle_step(w, probe)
+    t256 = max(time.perf_counter() - t, 1e-3)
+    growth = 0.5 if w.causal else 1.0
+    rows = int(256 * (budget / t256) ** growth) // 128 * 128
+    rows = max(128, min(rows, 2048, w.T))
+    sub, flop, desc = oracle_sample(w, x, rows)
+    for _ in range(args.warmup):
+        run_oracle_step(w, sub)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(w, sub)
+    dt = (time.perf_counter() - t) / max(args.steps, 1)
+    value = round(flop / dt / 1e12, 6)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "G": w.G, "T": w.T, "S": w.S,
+                   "H": w.H, "causal": w.causal, "segments": w.segments,
+                   "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, world, rank, local):
+    from flash_attention_gqa_gb300 import binding
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = binding.load()
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.make_workload(w)
+    seg_np = None if x.seg_q is None else x.seg_q.numpy()
+    fwd_flop, bwd_flop, frac = flop_counts(w, seg_np)
+    step_flop = fwd_flop + bwd_flop
+
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    dO = x.dO.to(dev) if w.backward else None
+    sq = None if x.seg_q is None else x.seg_q.to(dev)
+    skv = None if x.seg_kv is None else x.seg_kv.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.K, w.G, w.T), dtype=torch.float32, device=dev)
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(max(256, binding.fa_bwd_workspace_size(w.B, w.K, w.G, w.T, w.S, w.H)),
+                         dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    n_kernels = 1 + ((1 + (2 if sq is not None else 0) + 2) if w.backward else 0)
+    names = ["fa_fwd_kernel", "bwd_preprocess", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    n_ev = 5 if w.backward else 2
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        binding.fa_fwd(q, k, v, sq, skv, w.causal, o, lse, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        if w.backward:
+            for st in range(3):
+                binding.fa_bwd_stage(st, q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws,
+                                     stream)
+                if evs is not None:
+                    evs[2 + st].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert binding.fa_check_status(stream) == binding.FA_OK
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    status = binding.fa_check_status(stream)
+    assert status == binding.FA_OK, binding.status_string(status)
+    ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dev)
+
+    # per-kernel device time (mean over the timed steps)
+    per = {}
+    per["fa_fwd_kernel"] = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    if w.backward:
+        per["bwd_preprocess"] = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+        per["fa_bwd_dkdv_kernel"] = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
+        per["fa_bwd_dq_kernel"] = statistics.mean(e[3].elapsed_time(e[4]) for e in events)
+    # algorithmic FLOPs each kernel performs: fwd = S and O products; dK/dV = S,
+    # dP, dV, dK products (2x fwd); dQ = S, dP, dQ products (1.5x fwd)
+    kflop = {"fa_fwd_kernel": fwd_flop, "fa_bwd_dkdv_kernel": 2.0 * fwd_flop,
+             "fa_bwd_dq_kernel": 1.5 * fwd_flop}
+    top = max((n for n in per if n in kflop), key=lambda n: per[n])
+    burst, sustained, hbm, src = measured_peaks()
+    timed_s = ms * args.steps / 1e3
+    peak = burst if timed_s < 1.0 else sustained
+    achieved = kflop[top] / (per[top] * 1e-3) / 1e12
+    src_file = "fwd.cu" if top == "fa_fwd_kernel" else "bwd.cu"
+    tr = NCU_TRAFFIC.get(top)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(src_file) else None
+    roofline = {"bound": "tensor", "kernel": top, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "peak_source": f"{src} bf16 {'burst' if peak == burst else 'sustained'}",
+                "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
+
+    # end to end through the C ABI with host buffers: H2D inputs, D2H outputs
+    host_in = [t.pin_memory() for t in (x.q, x.k, x.v) + ((x.dO,) if w.backward else ())]
+    seg_host = [] if x.seg_q is None else [x.seg_q.pin_memory(), x.seg_kv.pin_memory()]
+    dev_in = [q, k, v] + ([dO] if w.backward else [])
+    dev_seg = [] if sq is None else [sq, skv]
+    outs = [o, lse] + ([dq, dk, dv] if w.backward else [])
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in + seg_host)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for h, d in zip(host_in + seg_host, dev_in + dev_seg):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dev)
+
+    in_bytes = sum(t.numel() * t.element_size() for t in dev_in + outs)
+    line = {
+        "metric": METRIC,
+        "value": round(world * step_flop / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; q pre-scaled by H^-1/2)",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "G": w.G, "T": w.T, "S": w.S,
+                   "H": w.H, "causal": w.causal, "segments": w.segments,
+                   "unmasked_frac": round(frac, 6), "fwd_flop": fwd_flop, "bwd_flop": bwd_flop,
+                   "fwd_tflops": round(fwd_flop / (per["fa_fwd_kernel"] * 1e-3) / 1e12, 1),
+                   "bwd_tflops": (round(bwd_flop / ((ms - per["fa_fwd_kernel"]) * 1e-3) / 1e12, 1)
+                                  if w.backward else None),
+                   "pct_of_peak": round(100 * step_flop / (ms * 1e-3) / 1e12 / peak, 2),
+                   "l2": f"inputs+outputs {in_bytes / 2**20:.0f} MiB vs L2 {L2_BYTES / 2**20:.0f} MiB"
+                         + (" (larger: no flush)" if in_bytes > L2_BYTES else " (smaller than L2)"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": round(world * step_flop / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": n_kernels * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            reference_arm(args, world, rank)
+        else:
+            ours_arm(args, world, rank, local)
+    finally:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -30,6 +30,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t,
                     _I, _I, _I, _I, _I, _I, _P]),
+    "fa_bwd_stage": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                          ctypes.c_size_t, _I, _I, _I, _I, _I, _I, _P]),
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
@@ -114,6 +116,20 @@ def fa_bwd(q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
                        _ptr(workspace), ws_bytes, B, K, G, T, S, H, _stream(stream))
     if check:
         _check("fa_bwd", rc)
+    return rc
+
+
+def fa_bwd_stage(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
+                 stream=None, check=True) -> int:
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_bwd_stage(int(stage), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                             _ptr(seg_q), _ptr(seg_kv), int(bool(causal)), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(workspace), ws_bytes, B, K, G, T, S, H,
+                             _stream(stream))
+    if check:
+        _check("fa_bwd_stage", rc)
     return rc
 
 

@@ -156,10 +156,14 @@ size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {
   return fa::bwd_workspace_bytes(B, K, G, T, S, H);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-           const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
-           void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
-           int S, int H, void* stream) {
+namespace {
+
+// Shared body of fa_bwd and fa_bwd_stage: stage < 0 runs every stage.
+int bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
+             void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
+             int S, int H, void* stream) {
+  if (stage < -1 || stage > 2) return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
   // Pointers are required (and must be aligned) only for tensors with elements.
@@ -183,9 +187,12 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (BK == 0) return FA_OK;
   if (rows == 0 || S == 0) {
     // No query rows or no keys: every gradient is zero.
-    if (rows > 0 && cudaMemsetAsync(dq, 0, (size_t)rows * H * 2, st) != cudaSuccess) return FA_ERR_CUDA;
-    if (S > 0 && (cudaMemsetAsync(dk, 0, (size_t)BK * S * H * 2, st) != cudaSuccess ||
-                  cudaMemsetAsync(dv, 0, (size_t)BK * S * H * 2, st) != cudaSuccess))
+    if ((stage < 0 || stage == 2) && rows > 0 &&
+        cudaMemsetAsync(dq, 0, (size_t)rows * H * 2, st) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if ((stage < 0 || stage == 1) && S > 0 &&
+        (cudaMemsetAsync(dk, 0, (size_t)BK * S * H * 2, st) != cudaSuccess ||
+         cudaMemsetAsync(dv, 0, (size_t)BK * S * H * 2, st) != cudaSuccess))
       return FA_ERR_CUDA;
     return FA_OK;
   }
@@ -205,12 +212,34 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
-  cudaError_t e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, st);
-  if (e == cudaSuccess) e = fa::launch_seg_ranges(a, st);
-  if (e == cudaSuccess) e = fa::launch_bwd_dkdv(a, st);
-  if (e == cudaSuccess) e = fa::launch_bwd_dq(a, st);
+  cudaError_t e = cudaSuccess;
+  if (stage < 0 || stage == 0) {
+    e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, st);
+    if (e == cudaSuccess) e = fa::launch_seg_ranges(a, st);
+  }
+  if (e == cudaSuccess && (stage < 0 || stage == 1)) e = fa::launch_bwd_dkdv(a, st);
+  if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq(a, st);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
+           void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
+           int S, int H, void* stream) {
+  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
+                  workspace_bytes, B, K, G, T, S, H, stream);
+}
+
+int fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, const int32_t* seg_q, const int32_t* seg_kv,
+                 int causal, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                 int B, int K, int G, int T, int S, int H, void* stream) {
+  if (stage < 0) return FA_ERR_INVALID_ARG;
+  return bwd_impl(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
+                  workspace_bytes, B, K, G, T, S, H, stream);
 }
 
 int fa_check_status(void* stream) {

@@ -89,6 +89,21 @@ int fa_bwd(const void* q, const void* k, const void* v,
            int B, int K, int G, int T, int S, int H, void* stream);
 
 /*
+ * One stage of fa_bwd, with the same arguments: stage 0 computes D and the
+ * per-tile segment ranges into the workspace, stage 1 writes dk and dv,
+ * stage 2 writes dq.  fa_bwd runs 0, 1, 2 in that order on `stream`; stages 1
+ * and 2 read only the inputs and stage 0's workspace, so a caller may run
+ * them on two streams once stage 0 is done.  Returns FA_ERR_INVALID_ARG for
+ * a stage outside 0..2.
+ */
+int fa_bwd_stage(int stage, const void* q, const void* k, const void* v,
+                 const void* o, const float* lse, const void* dO,
+                 const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                 void* dq, void* dk, void* dv,
+                 void* workspace, size_t workspace_bytes,
+                 int B, int K, int G, int T, int S, int H, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_CUDA.
  */
