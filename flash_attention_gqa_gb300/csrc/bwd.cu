@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
           waited_q = true;
         }
         const int u = n % NBUF;
-        if (n >= NBUF && !mbar_wait(dq_done(u), ((n / NBUF) - 1) & 1, ab)) { ok = false; break; }
-        tc_fence_after();
+        // Buffer u held S/dP(n-NBUF) (read by the softmax side before it signalled
+        // dS) and dS(n-NBUF) (read by dQ(n-NBUF), issued earlier by this thread;
+        // tcgen05.mma ops of one thread execute in issue order).
         for (int c = 0; c < HC && ok; ++c) {  // S = Q K^T
           const uint32_t sq = (uint32_t)n * HC + c;
           const int slot = sq % KSL;
@@ -346,8 +347,8 @@ struct DkvCfg {
   static constexpr uint32_t p_off = do_off + HC * kQChunk;
   static constexpr uint32_t ds_off = p_off + PC * kQChunk;
   static constexpr uint32_t bar_off = ds_off + PC * kQChunk;
-  // kv_full, q_full, q_empty, sdp_full, ps_full, teardown
-  static constexpr uint32_t misc_off = bar_off + 6 * 8;
+  // kv_full, q_empty, do_empty, sdp_full, ps_full, teardown, q_full[HC], do_full[HC]
+  static constexpr uint32_t misc_off = bar_off + (6 + 2 * HC) * 8;
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
   static constexpr uint32_t dv_col = 0;
   static constexpr uint32_t dk_col = HH * BN;
@@ -364,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar0 = sbase + C::bar_off;
-  const uint32_t kv_full = bar0, q_full = bar0 + 8, q_empty = bar0 + 16, sdp_full = bar0 + 24,
+  const uint32_t kv_full = bar0, q_empty = bar0 + 8, do_empty = bar0 + 16, sdp_full = bar0 + 24,
                  ps_full = bar0 + 32, teardown = bar0 + 40;
+  auto q_full = [&](int c) { return bar0 + 8 * (6 + c); };
+  auto do_full = [&](int c) { return bar0 + 8 * (6 + HC + c); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
   const Abort ab{abort_flag, a.wait_limit_ns, a.err};
@@ -382,11 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
+    mbar_init(do_empty, 1);
     mbar_init(sdp_full, 1);
     mbar_init(ps_full, kRows);
     mbar_init(teardown, 1);
+    for (int c = 0; c < HC; ++c) { mbar_init(q_full(c), 1); mbar_init(do_full(c), 1); }
     fence_barrier_init();
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
@@ -396,9 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
+    // Producer: K, V once; per Q tile, dO (released after dV^T) then Q
+    // (released after dK^T), one barrier per 64-dim chunk.
     if (lane == 0) {
       bool ok = true, any = false;
       int i = 0;
+      uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
         if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!any) {
@@ -409,15 +416,29 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
             tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
           }
         }
-        if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
-        mbar_arrive_expect_tx(q_full, 2 * HC * kQChunk);
+        issued = 0;
+        if (i > 0 && !mbar_wait(do_empty, (i - 1) & 1, ab)) { ok = false; break; }
         for (int c = 0; c < HC; ++c) {
-          tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full, c * 64, qt * Tb, 0, bk);
-          tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, q_full, c * 64, qt * Tb, 0, bk);
+          mbar_arrive_expect_tx(do_full(c), kQChunk);
+          tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, do_full(c), c * 64, qt * Tb, 0, bk);
+          issued |= 1u << (HC + c);
+        }
+        if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
+        for (int c = 0; c < HC; ++c) {
+          mbar_arrive_expect_tx(q_full(c), kQChunk);
+          tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(c), c * 64, qt * Tb, 0, bk);
+          issued |= 1u << c;
         }
         ++i;
       }
-      if (!ok && i > 0) mbar_wait_teardown(q_full, (i - 1) & 1, a.wait_limit_ns);
+      if (!ok) {
+        // Let the copies of the tile being loaded land before the CTA exits.
+        const int last = ok ? i - 1 : i;
+        for (int c = 0; c < HC; ++c) {
+          if (issued & (1u << c)) mbar_wait_teardown(q_full(c), last & 1, a.wait_limit_ns);
+          if (issued & (1u << (HC + c))) mbar_wait_teardown(do_full(c), last & 1, a.wait_limit_ns);
+        }
+      }
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -428,35 +449,46 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
         if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
-        if (!mbar_wait(q_full, i & 1, ab)) { ok = false; break; }
-        // S / dP TMEM is free once the softmax side has read the previous tile.
-        if (i > 0 && !mbar_wait(ps_full, (i - 1) & 1, ab)) { ok = false; break; }
-        tc_fence_after();
-        for (int c = 0; c < HC; ++c) {
-          const uint32_t qc = sbase + C::q_off + c * kQChunk, kc = sbase + C::k_off + c * C::KV_CHUNK;
+        // S / dP TMEM of the previous tile was read before the softmax side
+        // signalled ps_full, which this thread waited for before dV^T / dK^T.
+        for (int c = 0; c < HC && ok; ++c) {  // dP = dO V^T, chunk by chunk as dO lands
+          if (!mbar_wait(do_full(c), i & 1, ab)) { ok = false; break; }
+          tc_fence_after();
           const uint32_t dc = sbase + C::do_off + c * kQChunk, vc = sbase + C::v_off + c * C::KV_CHUNK;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ss(tmem + C::s_col, sdesc_sw128(qc + kk * 32, 16, 1024), sdesc_sw128(kc + kk * 32, 16, 1024),
-                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
             mma_ss(tmem + C::dp_col, sdesc_sw128(dc + kk * 32, 16, 1024), sdesc_sw128(vc + kk * 32, 16, 1024),
                    id_s, (c > 0 || kk > 0) ? 1u : 0u);
-          }
         }
+        for (int c = 0; c < HC && ok; ++c) {  // S = Q K^T
+          if (!mbar_wait(q_full(c), i & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qc = sbase + C::q_off + c * kQChunk, kc = sbase + C::k_off + c * C::KV_CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::s_col, sdesc_sw128(qc + kk * 32, 16, 1024), sdesc_sw128(kc + kk * 32, 16, 1024),
+                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
         mma_commit(sdp_full);
         if (!mbar_wait(ps_full, i & 1, ab)) { ok = false; break; }
         tc_fence_after();
-        for (int h = 0; h < HH; ++h) {
+        for (int h = 0; h < HH; ++h) {  // dV^T += dO^T P  (contraction over 128 query rows)
           const uint32_t dA = sbase + C::do_off + 2 * h * kQChunk;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::dv_col + h * BN, sdesc_sw128(dA + kk * 2048, kQChunk, 1024),
+                   sdesc_sw128(sbase + C::p_off + kk * 2048, kQChunk, 1024), id_t,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(do_empty);
+        for (int h = 0; h < HH; ++h) {  // dK^T += Q^T dS
           const uint32_t qA = sbase + C::q_off + 2 * h * kQChunk;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // contraction over the 128 packed query rows
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            mma_ss(tmem + C::dv_col + h * BN, sdesc_sw128(dA + kk * 2048, kQChunk, 1024),
-                   sdesc_sw128(sbase + C::p_off + kk * 2048, kQChunk, 1024), id_t, acc);
+          for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::dk_col + h * BN, sdesc_sw128(qA + kk * 2048, kQChunk, 1024),
-                   sdesc_sw128(sbase + C::ds_off + kk * 2048, kQChunk, 1024), id_t, acc);
-          }
+                   sdesc_sw128(sbase + C::ds_off + kk * 2048, kQChunk, 1024), id_t,
+                   (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(q_empty);
         ++i;
@@ -481,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const float Dr = a.delta[row];
       const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
       if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
-      // P / dS shared buffers are free once the previous tile's dV, dK products are done.
+      // P / dS shared buffers are free once the previous tile's dV^T, dK^T are done
+      // (q_empty is committed after both).
       if (i > 0 && !warp_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1

@@ -67,6 +67,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
   return __all_sync(0xffffffffu, ok);
 }
 
+// K/V chunks travel through the ring in the order the MMA warp consumes them:
+// K(0), K(1), V(0), K(2), V(1), ..., K(N-1), V(N-2), V(N-1).  Unit u holds the
+// H/64 chunks of one K or V tile; chunk c of unit u has sequence number u*HC+c.
+__device__ __forceinline__ uint32_t unit_k(int n) { return n == 0 ? 0u : (uint32_t)(2 * n - 1); }
+__device__ __forceinline__ uint32_t unit_v(int n, int n_tiles) {
+  return (uint32_t)min(2 * n + 2, 2 * n_tiles - 1);
+}
+
 // Tile classes of the lazy mask.
 enum : uint8_t { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
 
@@ -189,20 +197,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tma_load_4d(sbase + L::q_off + c * kChunkBytes, &a.tm_q, bars.q_full(), c * 64, t0, 0, bk);
       uint32_t seq = 0;
       bool ok = true;
-      for (int n = 0; n < n_tiles && ok; ++n) {
+      for (int u = 0; u < 2 * n_tiles && ok; ++u) {
+        // unit 0: K(0); last unit: V(N-1); odd u: K((u+1)/2); even u: V(u/2 - 1)
+        bool is_k;
+        int n;
+        if (u == 0) { is_k = true; n = 0; }
+        else if (u == 2 * n_tiles - 1) { is_k = false; n = n_tiles - 1; }
+        else if (u & 1) { is_k = true; n = (u + 1) / 2; }
+        else { is_k = false; n = u / 2 - 1; }
         const int j = tiles[n] & 0x7fff;
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          const CUtensorMap* m = kv == 0 ? &a.tm_k : &a.tm_v;
-          for (int c = 0; c < HC; ++c, ++seq) {
-            const int slot = seq % kSlots;
-            if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
-            tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
-                        j * kKvRows, bk);
+        const CUtensorMap* m = is_k ? &a.tm_k : &a.tm_v;
+        for (int c = 0; c < HC; ++c, ++seq) {
+          const int slot = seq % kSlots;
+          if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
+          tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
+                      j * kKvRows, bk);
         }
       }
       if (!ok) {
@@ -223,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t p_col = 256 + 128 * (n & 1);
         for (int c = 0; c < HC; ++c) {
-          const uint32_t seq = (uint32_t)n * 2 * HC + HC + c;
+          const uint32_t seq = unit_v(n, n_tiles) * HC + c;
           const int slot = seq % kSlots;
           if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) return false;
           tc_fence_after();
@@ -239,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         return true;
       };
       for (int n = 0; n < n_tiles && ok; ++n) {
-        // S buffer n&1 (and the P inside it) is free once O += P V of tile n-2 is done.
-        if (n >= 2 && !mbar_wait(bars.pv_done(n & 1), ((n - 2) >> 1) & 1, ab)) { ok = false; break; }
-        tc_fence_after();
+        // S buffer n&1 held S(n-2), read by the softmax warps before they signalled
+        // P(n-2), and P(n-2), read by O += P V of tile n-2, which this thread issued
+        // before S(n): tcgen05.mma ops of one thread execute in issue order.
         const uint32_t s_col = 256 + 128 * (n & 1);
         for (int c = 0; c < HC && ok; ++c) {
-          const uint32_t seq = (uint32_t)n * 2 * HC + c;
+          const uint32_t seq = unit_k(n) * HC + c;
           const int slot = seq % kSlots;
           if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) { ok = false; break; }
           tc_fence_after();
@@ -309,9 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
         }
       }
-      float mx = s[0];
+      // Row max with 8 independent partial maxima (short dependency chains).
+      float pm[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) pm[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pm[i] = fmaxf(pm[i], s[c + i]);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float m_tile = mx * kLog2e;
       float alpha = 1.f;
       bool rescale = false;
@@ -323,16 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         rescale = true;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(s[2 * c], kLog2e, -m_use));
-        const float p1 = fast_exp2(fmaf(s[2 * c + 1], kLog2e, -m_use));
-        sum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + sum;
       // O must be rescaled before O += P V of this tile; it holds every earlier tile.
       if (__any_sync(0xffffffffu, rescale)) {
         if (!warp_wait(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab)) { ok = false; break; }
@@ -347,8 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_st32(tmem + lane_base + c, ov);
         }
       }
-      tmem_st32(tmem + lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tmem + lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      // P = exp2(S log2e - m) in two halves of 64 keys; bf16 pairs overwrite the
+      // first 64 columns of this tile's S buffer (already read into registers).
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = fast_exp2(fmaf(s[64 * hf + 2 * c], kLog2e, -m_use));
+          const float p1 = fast_exp2(fmaf(s[64 * hf + 2 * c + 1], kLog2e, -m_use));
+          ps[c & 3] += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tmem + lane_base + s_col + 32 * hf, pk);
+      }
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.p_full(n & 1));
