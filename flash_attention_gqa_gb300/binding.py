@@ -32,6 +32,8 @@ SIGNATURES = {
                     _I, _I, _I, _I, _I, _I, _P]),
     "fa_bwd_stage": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                           ctypes.c_size_t, _I, _I, _I, _I, _I, _I, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
+                            _I, _I, _I, _I, _I, _I, _P]),
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
@@ -130,6 +132,19 @@ def fa_bwd_stage(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, 
                              _stream(stream))
     if check:
         _check("fa_bwd_stage", rc)
+    return rc
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, stream=None,
+                   check=True) -> int:
+    """fa_bwd with the library's fixed scratch instead of a caller workspace."""
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    rc = load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                               _ptr(seg_q), _ptr(seg_kv), int(bool(causal)), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, K, G, T, S, H, _stream(stream))
+    if check:
+        _check("fa_bwd_noalloc", rc)
     return rc
 
 

@@ -242,6 +242,45 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const v
                   workspace_bytes, B, K, G, T, S, H, stream);
 }
 
+// ------------------------------------------------------------------------
+// fa_bwd_noalloc: fa_bwd for callers that may not allocate device memory.
+// Its scratch is this fixed array; the host only ever uses the array's device
+// address, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* noalloc_scratch_address() {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                   void* dq, void* dk, void* dv, int B, int K, int G, int T, int S, int H,
+                   void* stream) {
+  const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
+  if (rc != FA_OK) return rc;
+  if (fa_bwd_workspace_size(B, K, G, T, S, H) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
+    return FA_ERR_UNSUPPORTED;
+  void* scratch = noalloc_scratch_address();
+  if (scratch == nullptr) return FA_ERR_CUDA;
+  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, scratch,
+                  (size_t)FA_NOALLOC_SCRATCH_BYTES, B, K, G, T, S, H, stream);
+}
+
 int fa_check_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   uint32_t err = 0;

@@ -103,6 +103,38 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v,
                  void* workspace, size_t workspace_bytes,
                  int B, int K, int G, int T, int S, int H, void* stream);
 
+/* Size of the fixed device scratch used by fa_bwd_noalloc (8 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory themselves: for example a plugin running inside a host
+ * application that owns every device allocation and offers no allocator
+ * hook, or a runtime whose rules forbid allocating after start-up.  It
+ * computes exactly what fa_bwd computes and calls no cudaMalloc, cudaFree or
+ * other allocating routine.  The pages have no counterpart to this call.
+ *
+ * The scratch (fp32 D rows plus per-tile segment ranges, the same data fa_bwd
+ * keeps in its workspace) is one fixed array of FA_NOALLOC_SCRATCH_BYTES in
+ * the library's device memory, present on every GPU that loads the library
+ * until the process exits.  Sizes whose scratch would not fit
+ * (fa_bwd_workspace_size(...) > FA_NOALLOC_SCRATCH_BYTES, i.e. roughly
+ * B*K*G*T > 2 million query rows) are rejected with FA_ERR_UNSUPPORTED before
+ * anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array and every call overwrites all of the scratch it reads,
+ * so nothing has to start at zero; but two calls that overlap on the GPU
+ * (different streams, not ordered) race on the array and give wrong results.
+ * Other arguments and status codes are those of fa_bwd.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v,
+                   const void* o, const float* lse, const void* dO,
+                   const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                   void* dq, void* dk, void* dv,
+                   int B, int K, int G, int T, int S, int H, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_CUDA.
