@@ -135,7 +135,7 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
   fa::FwdArgs a{};
   const int BK = B * K;
   if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
-      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows))
+      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows) || !make_q_map(&a.tm_o, o, BK, G, T, H))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
@@ -198,7 +198,8 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   }
   fa::BwdArgs a{};
   if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_q_map(&a.tm_do, dO, BK, G, T, H) ||
-      !make_kv_map(&a.tm_k, k, BK, S, H, kvr) || !make_kv_map(&a.tm_v, v, BK, S, H, kvr))
+      !make_kv_map(&a.tm_k, k, BK, S, H, kvr) || !make_kv_map(&a.tm_v, v, BK, S, H, kvr) ||
+      !make_q_map(&a.tm_dq, dq, BK, G, T, H))
     return FA_ERR_CUDA;
   float* delta = static_cast<float*>(workspace);
   a.lse = lse;

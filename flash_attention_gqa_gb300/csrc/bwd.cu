@@ -24,7 +24,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // 4 softmax-side warps, producer, two MMA issuers
 constexpr uint32_t kQChunk = 128 * 128;  // [128 rows x 64 dims] bf16
 constexpr float kLog2e = 1.4426950408889634f;
 enum : int { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
@@ -91,8 +91,8 @@ struct DqCfg {
   static constexpr uint32_t k_off = 2 * HC * kQChunk;
   static constexpr uint32_t v_off = k_off + KSL * KV_CHUNK;
   static constexpr uint32_t bar_off = v_off + VSL * KV_CHUNK;
-  // q_full, kfull[KSL], kempty[KSL], vfull[VSL], vempty[VSL], sdp_full[2], ds_full[2], dq_done[2], teardown
-  static constexpr int n_bars = 1 + 2 * KSL + 2 * VSL + 7;
+  // q_full, kfull[KSL], kempty[KSL], vfull[VSL], vempty[VSL], sdp_full[2], ds_full[2], dq_done[2], teardown[2]
+  static constexpr int n_bars = 1 + 2 * KSL + 2 * VSL + 8;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
   __host__ __device__ static constexpr uint32_t s_col(int u) { return H + u * 2 * BN; }
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   auto sdp_full = [&](int u) { return bar0 + 8 * (xb + u); };
   auto ds_full = [&](int u) { return bar0 + 8 * (xb + 2 + u); };
   auto dq_done = [&](int u) { return bar0 + 8 * (xb + 4 + u); };
-  const uint32_t teardown = bar0 + 8 * (xb + 6);
+  auto teardown = [&](int i) { return bar0 + 8 * (xb + 6 + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
   const Abort ab{abort_flag, a.wait_limit_ns, a.err};
@@ -139,11 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     for (int s = 0; s < KSL; ++s) { mbar_init(kfull(s), 1); mbar_init(kempty(s), 1); }
     for (int s = 0; s < VSL; ++s) { mbar_init(vfull(s), 1); mbar_init(vempty(s), 1); }
     for (int u = 0; u < 2; ++u) {
-      mbar_init(sdp_full(u), 1);
+      mbar_init(sdp_full(u), 2);  // S (issuer A) and dP (issuer B)
       mbar_init(ds_full(u), kRows);
       mbar_init(dq_done(u), 1);
     }
-    mbar_init(teardown, 1);
+    mbar_init(teardown(0), 1);
+    mbar_init(teardown(1), 1);
     fence_barrier_init();
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
@@ -195,26 +196,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       }
     }
   } else if (warp == 5) {
+    // Issuer A: S = Q K^T and dQ += dS K (both read the K ring).
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);
-      constexpr uint32_t id_q = idesc_bf16(128, 64, false, true);
+      constexpr uint32_t id_q = idesc_bf16(128, H, false, true);  // dQ += dS K, N = H
+      const uint64_t dqd = sdesc_sw128(sbase + C::q_off, 16, 1024);
+      const uint64_t dkk = sdesc_sw128(sbase + C::k_off, 16, 1024);                  // K, K-major
+      const uint64_t dkm = sdesc_sw128(sbase + C::k_off, C::KV_CHUNK, 1024);         // K, MN-major
       bool ok = true, waited_q = false;
       int n = 0;
-      // Issue dQ(m) += dS(m) K(m) for the m-th processed tile.
+      // dQ(m) += dS(m) K(m); the HC chunks of K(m) sit in consecutive ring
+      // slots, so one N = H product per 16 keys.
       auto issue_dq = [&](int m) -> bool {
         const int u = m % NBUF;
         if (!mbar_wait(ds_full(u), (m / NBUF) & 1, ab)) return false;
         tc_fence_after();
-        for (int c = 0; c < HC; ++c) {
-          const uint32_t sq = (uint32_t)m * HC + c;
-          const int slot = sq % KSL;
-          const uint32_t kb = sbase + C::k_off + slot * C::KV_CHUNK;
+        const int slot0 = (m * HC) % KSL;
+        const uint64_t b0 = sdesc_add(dkm, slot0 * C::KV_CHUNK);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + c * 64, tmem + C::s_col(u) + kk * 8, sdesc_sw128(kb + kk * 2048, C::KV_CHUNK, 1024),
-                   id_q, (m > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(kempty(slot));
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem, tmem + C::s_col(u) + kk * 8, sdesc_add(b0, kk * 2048), id_q,
+                 (m > 0 || kk > 0) ? 1u : 0u);
+        for (int c = 0; c < HC; ++c) mma_commit(kempty(slot0 + c));
         mma_commit(dq_done(u));
         return true;
       };
@@ -225,33 +228,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
           waited_q = true;
         }
         const int u = n % NBUF;
-        // Buffer u held S/dP(n-NBUF) (read by the softmax side before it signalled
-        // dS) and dS(n-NBUF) (read by dQ(n-NBUF), issued earlier by this thread;
-        // tcgen05.mma ops of one thread execute in issue order).
-        for (int c = 0; c < HC && ok; ++c) {  // S = Q K^T
+        // S columns of buffer u held dS(n-NBUF), read by dQ(n-NBUF), which this
+        // thread issued earlier (tcgen05.mma ops of one thread run in order).
+        for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = (uint32_t)n * HC + c;
           const int slot = sq % KSL;
           if (!mbar_wait(kfull(slot), (sq / KSL) & 1, ab)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t qc = sbase + C::q_off + c * kQChunk;
-          const uint32_t kc = sbase + C::k_off + slot * C::KV_CHUNK;
+          const uint64_t qa = sdesc_add(dqd, c * kQChunk), kb = sdesc_add(dkk, slot * C::KV_CHUNK);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + C::s_col(u), sdesc_sw128(qc + kk * 32, 16, 1024),
-                   sdesc_sw128(kc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        for (int c = 0; c < HC && ok; ++c) {  // dP = dO V^T
-          const uint32_t sq = (uint32_t)n * HC + c;
-          const int slot = sq % VSL;
-          if (!mbar_wait(vfull(slot), (sq / VSL) & 1, ab)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t dc = sbase + C::do_off + c * kQChunk;
-          const uint32_t vc = sbase + C::v_off + slot * C::KV_CHUNK;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + C::dp_col(u), sdesc_sw128(dc + kk * 32, 16, 1024),
-                   sdesc_sw128(vc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(vempty(slot));
+            mma_ss(tmem + C::s_col(u), sdesc_add(qa, kk * 32), sdesc_add(kb, kk * 32), id_s,
+                   (c > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(sdp_full(u));
@@ -261,8 +249,48 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       for (int m = n - (NBUF - 1); ok && m < n; ++m)
         if (m >= 0 && !issue_dq(m)) ok = false;
       if (!ok) {
-        mma_commit(teardown);
-        mbar_wait_teardown(teardown, 0, a.wait_limit_ns);
+        mma_commit(teardown(0));
+        mbar_wait_teardown(teardown(0), 0, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 6) {
+    // Issuer B: dP = dO V^T.
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);
+      const uint64_t ddo = sdesc_sw128(sbase + C::do_off, 16, 1024);
+      const uint64_t dvk = sdesc_sw128(sbase + C::v_off, 16, 1024);
+      bool ok = true, waited_q = false;
+      int n = 0;
+      for (int jt = 0; jt < jt_end && ok; ++jt) {
+        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (!waited_q) {
+          if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
+          waited_q = true;
+        }
+        const int u = n % NBUF;
+        // dP columns of buffer u are free once the softmax side has read dP(n-NBUF)
+        // (it signals ds_full after reading).
+        if (n >= NBUF && !mbar_wait(ds_full(u), ((n / NBUF) - 1) & 1, ab)) { ok = false; break; }
+        tc_fence_after();
+        for (int c = 0; c < HC && ok; ++c) {
+          const uint32_t sq = (uint32_t)n * HC + c;
+          const int slot = sq % VSL;
+          if (!mbar_wait(vfull(slot), (sq / VSL) & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = sdesc_add(ddo, c * kQChunk), vb = sdesc_add(dvk, slot * C::KV_CHUNK);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::dp_col(u), sdesc_add(da, kk * 32), sdesc_add(vb, kk * 32), id_s,
+                   (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(vempty(slot));
+        }
+        if (!ok) break;
+        mma_commit(sdp_full(u));
+        ++n;
+      }
+      if (!ok) {
+        mma_commit(teardown(1));
+        mbar_wait_teardown(teardown(1), 0, a.wait_limit_ns);
       }
     }
   } else {
@@ -307,24 +335,35 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       mbar_arrive(ds_full(u));
       ++n;
     }
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + row * H;
+    // dQ in bf16 is staged in the Q tile's shared memory (every MMA is done)
+    // with the Q box's swizzled layout and written by TMA stores.
     const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) % NBUF), ((n - 1) / NBUF) & 1, ab);
-    if (have) {
-      tc_fence_after();
+    if (have) tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < H; c += 32) {
-        uint32_t v[32];
+    for (int c = 0; c < H; c += 32) {
+      uint32_t v[32];
+      if (have) {
         tmem_ld32(tmem + lane_base + c, v);
         tmem_wait_ld();
-        uint4 pk[4];
-        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst + c)[i] = pk[i];
+        for (int i = 0; i < 32; ++i) v[i] = 0;
       }
-    } else {
-      for (int c = 0; c < H; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+      uint4 pk[4];
+      uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      uint8_t* chunk = sm + C::q_off + (c / 64) * kQChunk;
+      const uint32_t u0 = (c % 64) / 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pk[i];
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRows);
+    if (tid == 0) {
+      for (int c = 0; c < HC; ++c) tma_store_4d(&a.tm_dq, sbase + C::q_off + c * kQChunk, c * 64, t0, 0, bk);
+      bulk_commit();
+      bulk_wait_read0();
     }
   }
   tc_fence_before();
@@ -347,8 +386,8 @@ struct DkvCfg {
   static constexpr uint32_t p_off = do_off + HC * kQChunk;
   static constexpr uint32_t ds_off = p_off + PC * kQChunk;
   static constexpr uint32_t bar_off = ds_off + PC * kQChunk;
-  // kv_full, q_empty, do_empty, sdp_full, ps_full, teardown, q_full[HC], do_full[HC]
-  static constexpr uint32_t misc_off = bar_off + (6 + 2 * HC) * 8;
+  // kv_full, sdp_full, ps_full, teardown[2], q_full[HC], do_full[HC], q_empty[HH], do_empty[HH]
+  static constexpr uint32_t misc_off = bar_off + (5 + 2 * HC + 2 * HH) * 8;
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
   static constexpr uint32_t dv_col = 0;
   static constexpr uint32_t dk_col = HH * BN;
@@ -365,10 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar0 = sbase + C::bar_off;
-  const uint32_t kv_full = bar0, q_empty = bar0 + 8, do_empty = bar0 + 16, sdp_full = bar0 + 24,
-                 ps_full = bar0 + 32, teardown = bar0 + 40;
-  auto q_full = [&](int c) { return bar0 + 8 * (6 + c); };
-  auto do_full = [&](int c) { return bar0 + 8 * (6 + HC + c); };
+  const uint32_t kv_full = bar0, sdp_full = bar0 + 8, ps_full = bar0 + 16;
+  auto teardown = [&](int i) { return bar0 + 8 * (3 + i); };
+  auto q_full = [&](int c) { return bar0 + 8 * (5 + c); };
+  auto do_full = [&](int c) { return bar0 + 8 * (5 + HC + c); };
+  // Q (dO) 128-dim half h is released once dK^T (dV^T) of that half is done.
+  auto q_empty = [&](int h) { return bar0 + 8 * (5 + 2 * HC + h); };
+  auto do_empty = [&](int h) { return bar0 + 8 * (5 + 2 * HC + HH + h); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
   const Abort ab{abort_flag, a.wait_limit_ns, a.err};
@@ -385,11 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(kv_full, 1);
-    mbar_init(q_empty, 1);
-    mbar_init(do_empty, 1);
-    mbar_init(sdp_full, 1);
+    for (int h = 0; h < HH; ++h) { mbar_init(q_empty(h), 1); mbar_init(do_empty(h), 1); }
+    mbar_init(sdp_full, 2);  // S (issuer A) and dP (issuer B)
     mbar_init(ps_full, kRows);
-    mbar_init(teardown, 1);
+    mbar_init(teardown(0), 1);
+    mbar_init(teardown(1), 1);
     for (int c = 0; c < HC; ++c) { mbar_init(q_full(c), 1); mbar_init(do_full(c), 1); }
     fence_barrier_init();
   }
@@ -417,18 +459,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
           }
         }
         issued = 0;
-        if (i > 0 && !mbar_wait(do_empty, (i - 1) & 1, ab)) { ok = false; break; }
-        for (int c = 0; c < HC; ++c) {
-          mbar_arrive_expect_tx(do_full(c), kQChunk);
-          tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, do_full(c), c * 64, qt * Tb, 0, bk);
-          issued |= 1u << (HC + c);
+        for (int h = 0; h < HH && ok; ++h) {
+          if (i > 0 && !mbar_wait(do_empty(h), (i - 1) & 1, ab)) { ok = false; break; }
+          for (int c = 2 * h; c < 2 * h + 2; ++c) {
+            mbar_arrive_expect_tx(do_full(c), kQChunk);
+            tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, do_full(c), c * 64, qt * Tb, 0, bk);
+            issued |= 1u << (HC + c);
+          }
+          if (i > 0 && !mbar_wait(q_empty(h), (i - 1) & 1, ab)) { ok = false; break; }
+          for (int c = 2 * h; c < 2 * h + 2; ++c) {
+            mbar_arrive_expect_tx(q_full(c), kQChunk);
+            tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(c), c * 64, qt * Tb, 0, bk);
+            issued |= 1u << c;
+          }
         }
-        if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
-        for (int c = 0; c < HC; ++c) {
-          mbar_arrive_expect_tx(q_full(c), kQChunk);
-          tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(c), c * 64, qt * Tb, 0, bk);
-          issued |= 1u << c;
-        }
+        if (!ok) break;
         ++i;
       }
       if (!ok) {
@@ -440,62 +485,56 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 6) {
+    // Two MMA issuers: A (warp 5) issues S = Q K^T and dK^T += Q^T dS (the Q
+    // operand), B (warp 6) issues dP = dO V^T and dV^T += dO^T P (the dO operand).
     if (lane == 0) {
+      const bool is_a = warp == 5;
       constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);  // S, dP: [128 q x BN]
       constexpr uint32_t id_t = idesc_bf16(128, BN, true, true);    // dV^T, dK^T: [128 h x BN]
+      const uint32_t x_off = is_a ? C::q_off : C::do_off;            // Q or dO tile
+      const uint32_t y_off = is_a ? C::k_off : C::v_off;             // K or V tile
+      const uint32_t z_off = is_a ? C::ds_off : C::p_off;            // dS or P
+      const uint32_t d_col = is_a ? C::s_col : C::dp_col;            // S or dP
+      const uint32_t acc_col = is_a ? C::dk_col : C::dv_col;         // dK^T or dV^T
+
+      const uint64_t d_x = sdesc_sw128(sbase + x_off, 16, 1024);
+      const uint64_t d_y = sdesc_sw128(sbase + y_off, 16, 1024);
+      const uint64_t d_xT = sdesc_sw128(sbase + x_off, kQChunk, 1024);  // X^T, MN-major
+      const uint64_t d_z = sdesc_sw128(sbase + z_off, kQChunk, 1024);
       bool ok = true;
       int i = 0;
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
         if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
-        // S / dP TMEM of the previous tile was read before the softmax side
-        // signalled ps_full, which this thread waited for before dV^T / dK^T.
-        for (int c = 0; c < HC && ok; ++c) {  // dP = dO V^T, chunk by chunk as dO lands
-          if (!mbar_wait(do_full(c), i & 1, ab)) { ok = false; break; }
+        // This issuer's S (or dP) columns of the previous tile were read before
+        // the softmax side signalled ps_full, which it waited for below.
+        for (int c = 0; c < HC && ok; ++c) {
+          if (!mbar_wait(is_a ? q_full(c) : do_full(c), i & 1, ab)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t dc = sbase + C::do_off + c * kQChunk, vc = sbase + C::v_off + c * C::KV_CHUNK;
+          const uint64_t xa = sdesc_add(d_x, c * kQChunk), yb = sdesc_add(d_y, c * C::KV_CHUNK);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + C::dp_col, sdesc_sw128(dc + kk * 32, 16, 1024), sdesc_sw128(vc + kk * 32, 16, 1024),
-                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        for (int c = 0; c < HC && ok; ++c) {  // S = Q K^T
-          if (!mbar_wait(q_full(c), i & 1, ab)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qc = sbase + C::q_off + c * kQChunk, kc = sbase + C::k_off + c * C::KV_CHUNK;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + C::s_col, sdesc_sw128(qc + kk * 32, 16, 1024), sdesc_sw128(kc + kk * 32, 16, 1024),
-                   id_s, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + d_col, sdesc_add(xa, kk * 32), sdesc_add(yb, kk * 32), id_s,
+                   (c > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
         mma_commit(sdp_full);
         if (!mbar_wait(ps_full, i & 1, ab)) { ok = false; break; }
         tc_fence_after();
-        for (int h = 0; h < HH; ++h) {  // dV^T += dO^T P  (contraction over 128 query rows)
-          const uint32_t dA = sbase + C::do_off + 2 * h * kQChunk;
+        for (int h = 0; h < HH; ++h) {  // contraction over the 128 packed query rows
+          const uint64_t xA = sdesc_add(d_xT, 2 * h * kQChunk);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::dv_col + h * BN, sdesc_sw128(dA + kk * 2048, kQChunk, 1024),
-                   sdesc_sw128(sbase + C::p_off + kk * 2048, kQChunk, 1024), id_t,
+            mma_ss(tmem + acc_col + h * BN, sdesc_add(xA, kk * 2048), sdesc_add(d_z, kk * 2048), id_t,
                    (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(is_a ? q_empty(h) : do_empty(h));  // this half of Q (dO) is free
         }
-        mma_commit(do_empty);
-        for (int h = 0; h < HH; ++h) {  // dK^T += Q^T dS
-          const uint32_t qA = sbase + C::q_off + 2 * h * kQChunk;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::dk_col + h * BN, sdesc_sw128(qA + kk * 2048, kQChunk, 1024),
-                   sdesc_sw128(sbase + C::ds_off + kk * 2048, kQChunk, 1024), id_t,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(q_empty);
         ++i;
       }
       if (!ok) {
-        mma_commit(teardown);
-        mbar_wait_teardown(teardown, 0, a.wait_limit_ns);
+        mma_commit(teardown(is_a ? 0 : 1));
+        mbar_wait_teardown(teardown(is_a ? 0 : 1), 0, a.wait_limit_ns);
       }
     }
   } else {
@@ -513,9 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const float Dr = a.delta[row];
       const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
       if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
-      // P / dS shared buffers are free once the previous tile's dV^T, dK^T are done
-      // (q_empty is committed after both).
-      if (i > 0 && !warp_wait(q_empty, (i - 1) & 1, ab)) { ok = false; break; }
+      // P and dS shared buffers are free once the previous tile's dV^T and dK^T
+      // are done (the last half's release barriers follow every earlier product).
+      if (i > 0 && (!warp_wait(q_empty(HH - 1), (i - 1) & 1, ab) ||
+                    !warp_wait(do_empty(HH - 1), (i - 1) & 1, ab))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -550,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       ++i;
     }
     // Epilogue: lanes carry the head dim, columns the keys.
-    const bool have = i > 0 && ok && warp_wait(q_empty, (i - 1) & 1, ab);
+    const bool have = i > 0 && ok && warp_wait(q_empty(HH - 1), (i - 1) & 1, ab) &&
+                      warp_wait(do_empty(HH - 1), (i - 1) & 1, ab);
     if (have) tc_fence_after();
     __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
     __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;

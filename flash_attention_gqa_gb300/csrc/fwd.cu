@@ -229,25 +229,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
-      constexpr uint32_t id_o = idesc_bf16(128, 64, false, true);    // O[:, 64c:] += P V_c
+      constexpr uint32_t id_o = idesc_bf16(128, H, false, true);     // O += P V (N = H)
+      // Operand descriptors, built once and advanced by byte offsets.
+      const uint64_t dq0 = sdesc_sw128(sbase + L::q_off, 16, 1024);        // Q, K-major
+      const uint64_t dk0 = sdesc_sw128(sbase + L::ring_off, 16, 1024);     // K chunk, K-major
+      const uint64_t dv0 = sdesc_sw128(sbase + L::ring_off, kChunkBytes, 1024);  // V, MN-major
       bool ok = mbar_wait(bars.q_full(), 0, ab);
       auto issue_pv = [&](int n) -> bool {
         if (!mbar_wait(bars.p_full(n & 1), (n >> 1) & 1, ab)) return false;
+        const uint32_t seq0 = unit_v(n, n_tiles) * HC;
+        const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
+        for (int c = 0; c < HC; ++c)
+          if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) return false;
         tc_fence_after();
         const uint32_t p_col = 256 + 128 * (n & 1);
-        for (int c = 0; c < HC; ++c) {
-          const uint32_t seq = unit_v(n, n_tiles) * HC + c;
-          const int slot = seq % kSlots;
-          if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) return false;
-          tc_fence_after();
-          const uint32_t vbase = sbase + L::ring_off + slot * kChunkBytes;
+        const uint64_t bv = sdesc_add(dv0, slot0 * kChunkBytes);
 #pragma unroll
-          for (int kk = 0; kk < kKvRows / 16; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, kChunkBytes, 1024);
-            mma_ts(tmem + c * 64, tmem + p_col + kk * 8, bdesc, id_o, (n > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bars.empty(slot));
-        }
+        for (int kk = 0; kk < kKvRows / 16; ++kk)
+          mma_ts(tmem, tmem + p_col + kk * 8, sdesc_add(bv, kk * 2048), id_o,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        for (int c = 0; c < HC; ++c) mma_commit(bars.empty(slot0 + c));
         mma_commit(bars.pv_done(n & 1));
         return true;
       };
@@ -256,19 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         // P(n-2), and P(n-2), read by O += P V of tile n-2, which this thread issued
         // before S(n): tcgen05.mma ops of one thread execute in issue order.
         const uint32_t s_col = 256 + 128 * (n & 1);
+        const uint32_t seq0 = unit_k(n) * HC;
+        const int slot0 = seq0 % kSlots;
         for (int c = 0; c < HC && ok; ++c) {
-          const uint32_t seq = unit_k(n) * HC + c;
-          const int slot = seq % kSlots;
-          if (!mbar_wait(bars.full(slot), (seq / kSlots) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t qc = sbase + L::q_off + c * kChunkBytes;
-          const uint32_t kc = sbase + L::ring_off + slot * kChunkBytes;
+          const uint64_t a = sdesc_add(dq0, c * kChunkBytes);
+          const uint64_t bk_ = sdesc_add(dk0, (slot0 + c) * kChunkBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ss(tmem + s_col, sdesc_sw128(qc + kk * 32, 16, 1024),
-                   sdesc_sw128(kc + kk * 32, 16, 1024), id_s, (c > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bars.empty(slot));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + s_col, sdesc_add(a, kk * 32), sdesc_add(bk_, kk * 32), id_s,
+                   (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bars.empty(slot0 + c));
         }
         if (!ok) break;
         mma_commit(bars.s_full(n & 1));
@@ -379,32 +379,42 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_arrive(bars.p_full(n & 1));
     }
     // ------------------------------------------------------------ epilogue
+    // O / l in bf16 is staged in the Q tile's shared memory (free: every MMA
+    // has completed) in the same swizzled layout the Q box arrived in, then
+    // written by TMA stores.
     const long row = ((long)bk * a.G + g) * a.T + t;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + row * H;
     const bool have = n_tiles > 0 && ok &&
                       warp_wait(bars.pv_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, ab);
-    if (have) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (have) tc_fence_after();
+    const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < H; c += 32) {
-        uint32_t ov[32];
+    for (int c = 0; c < H; c += 32) {
+      uint32_t ov[32];
+      if (have) {
         tmem_ld32(tmem + lane_base + c, ov);
         tmem_wait_ld();
-        uint4 pkd[4];
-        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+        for (int i = 0; i < 32; ++i) ov[i] = 0;
       }
-      a.lse[row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-    } else {
-      uint4 z = make_uint4(0, 0, 0, 0);
-      for (int c = 0; c < H; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
-      a.lse[row] = -INFINITY;
+      uint4 pkd[4];
+      uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+      uint8_t* chunk = sm + L::q_off + (c / 64) * kChunkBytes;
+      const uint32_t u0 = (c % 64) / 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
+    }
+    a.lse[row] = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRows);
+    if (tid == 0) {
+      for (int c = 0; c < HC; ++c)
+        tma_store_4d(&a.tm_o, sbase + L::q_off + c * kChunkBytes, c * 64, t0, 0, bk);
+      bulk_commit();
+      bulk_wait_read0();
     }
   }
 

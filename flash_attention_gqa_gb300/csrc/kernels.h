@@ -15,6 +15,7 @@ struct FwdArgs {
   CUtensorMap tm_q;   // q as 4-D {H, T, G, B*K}, box {64, 128/G, G, 1}, 128B swizzle
   CUtensorMap tm_k;   // k as 3-D {H, S, B*K},   box {64, 128, 1}
   CUtensorMap tm_v;   // v, same as k
+  CUtensorMap tm_o;   // o, same geometry as q (TMA store of the finished tile)
   void* o;            // bf16 [B*K, G, T, H]
   float* lse;         // [B*K, G, T]
   const int32_t* seg_q;   // [B, T] or null
@@ -31,6 +32,7 @@ struct BwdArgs {
   CUtensorMap tm_do;   // dO as 4-D, same box
   CUtensorMap tm_k;    // k as 3-D, box {64, kv_rows, 1}
   CUtensorMap tm_v;    // v as 3-D, box {64, kv_rows, 1}
+  CUtensorMap tm_dq;   // dq as 4-D, same box as q (TMA store)
   const float* lse;    // [B*K, G, T]
   const float* delta;  // [B*K, G, T]  D = rowsum(dO * o)
   void* dq;            // bf16 [B*K, G, T, H]
