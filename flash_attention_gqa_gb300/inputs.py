@@ -144,10 +144,11 @@ def unmasked_pairs(T: int, S: int, causal: bool,
 
     This is bookkeeping for FLOP accounting (the mask-adjusted FLOP count),
     computed by counting, not by the attention arithmetic."""
+    off = S - T
     if seg_q is None:
         if causal:
-            # keep s <= t, same absolute index for queries and keys
-            per = sum(min(t + 1, S) for t in range(T))
+            # keep s <= t + (S - T): queries aligned to the end of the keys
+            per = sum(max(0, min(t + off + 1, S)) for t in range(T))
         else:
             per = T * S
         return per * B
@@ -159,7 +160,7 @@ def unmasked_pairs(T: int, S: int, causal: bool,
             tq = np.nonzero(sq == i)[0]
             ts = np.nonzero(sk == i)[0]
             if causal:
-                total += int(np.searchsorted(ts, tq, side="right").sum())
+                total += int(np.searchsorted(ts, tq + off, side="right").sum())
             else:
                 total += len(tq) * len(ts)
     return total

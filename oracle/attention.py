@@ -25,7 +25,9 @@ float64, on the bf16-rounded inputs:
       dk = sum_g dS^T . q,  dv = sum_g W^T . dO.
 
 Readings where the pages are silent (all listed with the design notes):
-  * causal keeps s <= t with the same absolute index for queries and keys;
+  * causal keeps s <= t + (S - T): queries are aligned to the end of the keys,
+    so the last query sees every key; for T == S this is s <= t with the same
+    absolute index for queries and keys (the pages only use T == S);
   * a query row with no kept key has O = 0, lse = -inf and contributes no
     gradient ("only the same id can attend" leaves it nothing to attend to);
   * natural exp/log throughout; lse is in natural-log units.
@@ -60,11 +62,13 @@ def _i32(x) -> Optional[np.ndarray]:
 
 def attention_mask(t_idx: np.ndarray, s_idx: np.ndarray, causal: bool,
                    seg_q_row: Optional[np.ndarray],
-                   seg_kv_row: Optional[np.ndarray]) -> np.ndarray:
-    """Boolean keep-mask M[t, s] for the given query and key positions."""
+                   seg_kv_row: Optional[np.ndarray], offset: int = 0) -> np.ndarray:
+    """Boolean keep-mask M[t, s] for the given query and key positions.
+
+    ``offset`` is S - T: with ``causal`` a query t keeps the keys s <= t + offset."""
     m = np.ones((len(t_idx), len(s_idx)), dtype=bool)
     if causal:
-        m &= s_idx[None, :] <= t_idx[:, None]
+        m &= s_idx[None, :] <= t_idx[:, None] + offset
     if seg_q_row is not None:
         m &= seg_q_row[t_idx][:, None] == seg_kv_row[s_idx][None, :]
     return m
@@ -91,10 +95,10 @@ def _row_blocks(T: int, rb: int):
         yield t0, min(T, t0 + rb)
 
 
-def _key_range(t1: int, S: int, causal: bool) -> int:
-    # keys s >= t1 are masked for every row t < t1 when causal; they would
-    # only contribute exact zeros, so the logits are not evaluated there.
-    return min(S, t1) if causal else S
+def _key_range(t1: int, S: int, causal: bool, offset: int = 0) -> int:
+    # keys s >= t1 + offset are masked for every row t < t1 when causal; they
+    # would only contribute exact zeros, so the logits are not evaluated there.
+    return max(0, min(S, t1 + offset)) if causal else S
 
 
 def attention_forward(q, k, v, *, causal: bool = False, seg_q=None,
@@ -112,13 +116,16 @@ def attention_forward(q, k, v, *, causal: bool = False, seg_q=None,
     lse = np.full((B, K, G, T), NEG_INF)
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(K)]
     s_all = np.arange(S)
+    off = S - T
     for b, kh in pairs:
         for t0, t1 in _row_blocks(T, row_block):
-            ns = _key_range(t1, S, causal)
+            ns = _key_range(t1, S, causal, off)
+            if ns == 0:       # no key is visible to these rows: O = 0, lse = -inf
+                continue
             t_idx = np.arange(t0, t1)
             M = attention_mask(t_idx, s_all[:ns], causal,
                                None if sq is None else sq[b],
-                               None if skv is None else skv[b])
+                               None if skv is None else skv[b], off)
             L = q[b, kh, :, t0:t1, :] @ k[b, kh, :ns, :].T       # [G, rb, ns]
             W, l = masked_softmax(L, M[None])
             o[b, kh, :, t0:t1, :] = W @ v[b, kh, :ns, :]
@@ -139,13 +146,16 @@ def attention_backward(q, k, v, dO, *, causal: bool = False, seg_q=None,
     dv = np.zeros_like(v)
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(K)]
     s_all = np.arange(S)
+    off = S - T
     for b, kh in pairs:
         for t0, t1 in _row_blocks(T, row_block):
-            ns = _key_range(t1, S, causal)
+            ns = _key_range(t1, S, causal, off)
+            if ns == 0:       # rows with no visible key contribute no gradient
+                continue
             t_idx = np.arange(t0, t1)
             M = attention_mask(t_idx, s_all[:ns], causal,
                                None if sq is None else sq[b],
-                               None if skv is None else skv[b])
+                               None if skv is None else skv[b], off)
             qb = q[b, kh, :, t0:t1, :]                            # [G, rb, H]
             dOb = dO[b, kh, :, t0:t1, :]
             L = qb @ k[b, kh, :ns, :].T                           # [G, rb, ns]
@@ -167,7 +177,7 @@ def attention_rows(q, k, v, b: int, kh: int, g: int, t_rows, *,
     S = k.shape[0]
     M = attention_mask(t_idx, np.arange(S), causal,
                        None if sq is None else sq[b],
-                       None if skv is None else skv[b])
+                       None if skv is None else skv[b], S - q.shape[0])
     W, l = masked_softmax(q[t_idx] @ k.T, M)
     return W @ v, l
 
@@ -190,9 +200,14 @@ def attention_backward_rows(q, k, v, dO, b: int, kh: int, *, t_rows, s_rows,
     lse = np.empty((G, T))
     delta = np.empty((G, T))
     s_all = np.arange(S)
+    off = S - T
     for t0, t1 in _row_blocks(T, row_block):
-        ns = _key_range(t1, S, causal)
-        M = attention_mask(np.arange(t0, t1), s_all[:ns], causal, sqb, skb)
+        ns = _key_range(t1, S, causal, off)
+        if ns == 0:
+            lse[:, t0:t1] = NEG_INF
+            delta[:, t0:t1] = 0.0
+            continue
+        M = attention_mask(np.arange(t0, t1), s_all[:ns], causal, sqb, skb, off)
         W, l = masked_softmax(qh[:, t0:t1] @ kk[:ns].T, M[None])
         dP = dOh[:, t0:t1] @ vv[:ns].T
         lse[:, t0:t1] = l
@@ -201,13 +216,13 @@ def attention_backward_rows(q, k, v, dO, b: int, kh: int, *, t_rows, s_rows,
     t_rows = np.asarray(t_rows)
     s_rows = np.asarray(s_rows)
     # dq rows: full key range for the sampled query rows
-    M = attention_mask(t_rows, s_all, causal, sqb, skb)
+    M = attention_mask(t_rows, s_all, causal, sqb, skb, off)
     Wt, _ = masked_softmax(qh[:, t_rows] @ kk.T, M[None])
     dPt = dOh[:, t_rows] @ vv.T
     dSt = Wt * (dPt - delta[:, t_rows][..., None])
     dq = dSt @ kk                                                   # [G, nt, H]
     # dk / dv rows: all queries against the sampled keys
-    M = attention_mask(np.arange(T), s_rows, causal, sqb, skb)      # [T, ns]
+    M = attention_mask(np.arange(T), s_rows, causal, sqb, skb, off)  # [T, ns]
     L = qh @ kk[s_rows].T                                           # [G, T, ns]
     fin = np.isfinite(lse)[..., None]
     Ws = np.where(M[None] & fin, np.exp(L - np.where(fin, lse[..., None], 0.0)), 0.0)
@@ -239,7 +254,7 @@ def attention_bruteforce(q, k, v, dO=None, *, causal: bool = False,
                 for t in range(T):
                     keep = []
                     for s in range(S):
-                        ok = (not causal) or s <= t
+                        ok = (not causal) or s <= t + (S - T)
                         if sq is not None:
                             ok = ok and sq[b, t] == skv[b, s]
                         if ok:

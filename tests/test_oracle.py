@@ -171,6 +171,30 @@ def test_blocked_matches_bruteforce(causal, segs):
     assert np.max(np.abs(lse[fin] - ref[1][fin])) <= 1e-12
 
 
+@pytest.mark.parametrize("T,S", [(3, 8), (8, 3), (5, 5), (1, 7)])
+@pytest.mark.parametrize("segs", [False, True])
+def test_rectangular_causal_bruteforce(T, S, segs):
+    # causal with T != S: queries aligned to the end of the keys (s <= t + S - T)
+    q, k, v, dO = small(B=1, K=2, G=2, T=T, S=S, H=4, seed=22 + T + S)
+    sq = skv = None
+    if segs:
+        sq = inputs.random_segment_ids(1, T, 2, seed=5)
+        skv = inputs.random_segment_ids(1, S, 2, seed=6)
+    kw = dict(causal=True, seg_q=sq, seg_kv=skv)
+    o, lse = oracle.attention_forward(q, k, v, row_block=2, **kw)
+    dq, dk, dv = oracle.attention_backward(q, k, v, dO, row_block=2, **kw)
+    ref = oracle.attention_bruteforce(q, k, v, dO, **kw)
+    for a, r in zip((o, dq, dk, dv), (ref[0], ref[2], ref[3], ref[4])):
+        assert np.max(np.abs(a - r)) <= 1e-12
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref[1]))
+    fin = np.isfinite(lse)
+    assert np.max(np.abs(lse[fin] - ref[1][fin]), initial=0.0) <= 1e-12
+    # the last query sees every key (when T <= S), the first S - T + 1 keys... etc.
+    if T <= S and not segs:
+        m = oa.attention_mask(np.arange(T), np.arange(S), True, None, None, S - T)
+        assert m[-1].all() and m[0].sum() == S - T + 1
+
+
 def test_rectangular_noncausal_bruteforce():
     q, k, v, dO = small(B=1, K=2, G=2, T=3, S=8, H=4, seed=21)
     o, lse = oracle.attention_forward(q, k, v)
@@ -217,7 +241,7 @@ def test_gradients_match_finite_differences(causal, segs):
 
 # ------------------------------------------- independent library routine
 
-def _sdpa_reference(q, k, v, dO, causal, seg):
+def _sdpa_reference(q, k, v, dO, causal, seg, seg_kv=None):
     """torch scaled_dot_product_attention in fp64 with autograd (scale 1 because
     q is pre-scaled); the kv heads are repeated over the G query heads."""
     B, K, G, T, H = q.shape
@@ -231,10 +255,12 @@ def _sdpa_reference(q, k, v, dO, causal, seg):
     if causal or seg is not None:
         m = torch.ones(B, 1, T, S, dtype=torch.bool)
         if causal:
-            m &= torch.ones(T, S, dtype=torch.bool).tril()
+            # end-aligned causal mask: keep s <= t + (S - T)
+            m &= torch.ones(T, S, dtype=torch.bool).tril(diagonal=S - T)
         if seg is not None:
-            s = torch.tensor(seg)
-            m &= (s[:, :, None] == s[:, None, :])[:, None]
+            sq = torch.tensor(seg)
+            sk = torch.tensor(seg if seg_kv is None else seg_kv)
+            m &= (sq[:, :, None] == sk[:, None, :])[:, None]
         mask = m
     o = torch.nn.functional.scaled_dot_product_attention(qt, ke, ve, attn_mask=mask,
                                                          scale=1.0)
@@ -255,6 +281,24 @@ def test_matches_torch_sdpa_fp64(causal, segs):
     ro, rdq, rdk, rdv = _sdpa_reference(q, k, v, dO, causal, seg)
     for a, r in ((o, ro), (dq, rdq), (dk, rdk), (dv, rdv)):
         assert np.max(np.abs(a - r)) <= 1e-12
+
+
+@pytest.mark.parametrize("T,S", [(24, 40), (40, 24)])
+def test_rectangular_causal_matches_torch_sdpa(T, S):
+    B, K, G, H = 1, 2, 2, 8
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((B, K, G, T, H)) * H ** -0.5
+    k = rng.standard_normal((B, K, S, H))
+    v = rng.standard_normal((B, K, S, H))
+    dO = rng.standard_normal((B, K, G, T, H))
+    o, _ = oracle.attention_forward(q, k, v, causal=True, row_block=7)
+    dq, dk, dv = oracle.attention_backward(q, k, v, dO, causal=True, row_block=7)
+    ro, rdq, rdk, rdv = _sdpa_reference(q, k, v, dO, True, None)
+    rows = slice(max(0, T - S), T)   # rows with at least one key (SDPA gives NaN otherwise)
+    assert np.max(np.abs(o[:, :, :, rows] - ro[:, :, :, rows])) <= 1e-12
+    assert np.max(np.abs(dq[:, :, :, rows] - rdq[:, :, :, rows])) <= 1e-12
+    if T <= S:
+        assert np.max(np.abs(dk - rdk)) <= 1e-12 and np.max(np.abs(dv - rdv)) <= 1e-12
 
 
 # ----------------------------------------------- sampled-row entry points
@@ -366,3 +410,6 @@ def test_unmasked_pair_count():
     assert n == brute
     assert inputs.unmasked_pairs(7, 7, True, None, None) == 28
     assert inputs.unmasked_pairs(7, 5, False, None, None) == 35
+    for T, S in ((3, 9), (9, 3)):
+        m = oa.attention_mask(np.arange(T), np.arange(S), True, None, None, S - T)
+        assert inputs.unmasked_pairs(T, S, True, None, None) == int(m.sum())
