@@ -102,11 +102,10 @@ int check_shapes(int B, int K, int G, int T, int S, int H, int causal, const voi
   if (B < 0 || K < 0 || G < 0 || T < 0 || S < 0 || H < 0) return FA_ERR_INVALID_ARG;
   if ((seg_q == nullptr) != (seg_kv == nullptr)) return FA_ERR_INVALID_ARG;
   if (seg_q && (!aligned16(seg_q) || !aligned16(seg_kv))) return FA_ERR_INVALID_ARG;
+  (void)causal;
   if (H != 64 && H != 128 && H != 256) return FA_ERR_UNSUPPORTED;
   if (!pow2_le128(G)) return FA_ERR_UNSUPPORTED;
-  if (T % kRows != 0 || S % fa::kKvRows != 0) return FA_ERR_UNSUPPORTED;
-  if (causal && T != S) return FA_ERR_UNSUPPORTED;
-  if (S / fa::kKvRows > fa::kMaxKvTiles) return FA_ERR_UNSUPPORTED;
+  if ((S + fa::kKvRows - 1) / fa::kKvRows > fa::kMaxKvTiles) return FA_ERR_UNSUPPORTED;
   if ((long long)B * K > 65535) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -143,7 +142,7 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
   a.seg_kv = seg_kv;
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
   a.causal = causal ? 1 : 0;
-  a.n_qtiles = T / (kRows / G);
+  a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
@@ -208,8 +207,8 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.seg_q = seg_q; a.seg_kv = seg_kv;
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
   a.causal = causal ? 1 : 0;
-  a.n_qtiles = T / (kRows / G);
-  a.n_kvtiles = S / kvr;
+  a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
+  a.n_kvtiles = (S + kvr - 1) / kvr;
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;

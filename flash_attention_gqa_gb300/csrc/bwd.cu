@@ -34,17 +34,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
   return __all_sync(0xffffffffu, ok);
 }
 
-// Mask class of the (Q tile, KV tile) pair; q tile covers positions
-// [t0, t0 + Tb), kv tile [s0, s0 + kvr).  Segment ranges come from the
-// per-tile [min, max] table (conservative for non-monotone ids).
+// Mask class of the (Q tile, KV tile) pair; the q tile covers positions
+// [t0, min(t0 + Tb, T)), the kv tile [s0, min(s0 + kvr, S)).  Causal keeps
+// s <= t + (S - T).  Segment ranges come from the per-tile [min, max] table
+// (conservative for non-monotone ids).  Keys past S on a ragged last tile
+// make it PARTIAL; query rows past T are handled by their -inf lse instead.
 __device__ __forceinline__ int tile_class(const BwdArgs& a, const int2* qr, const int2* kr, int b,
                                           int qt, int jt, int Tb, int kvr) {
   const int t0 = qt * Tb, s0 = jt * kvr;
+  const int t_last = min(t0 + Tb, a.T) - 1, s_last = min(s0 + kvr, a.S) - 1;
+  const int off = a.S - a.T;
   int c = TILE_FULL;
   if (a.causal) {
-    if (t0 + Tb - 1 < s0) return TILE_EMPTY;
-    if (t0 < s0 + kvr - 1) c = TILE_PARTIAL;
+    if (t_last + off < s0) return TILE_EMPTY;
+    if (t0 + off < s_last) c = TILE_PARTIAL;
   }
+  if (s0 + kvr > a.S) c = TILE_PARTIAL;
   if (a.seg_q != nullptr) {
     const int2 q = qr[(long)b * a.n_qtiles + qt];
     const int2 k = kr[(long)b * a.n_kvtiles + jt];
@@ -54,23 +59,47 @@ __device__ __forceinline__ int tile_class(const BwdArgs& a, const int2* qr, cons
   return c;
 }
 
-// Apply the causal / segment mask to 32 consecutive key columns of one row.
+// First Q tile a KV tile starting at s0 can see under the causal mask.
+__device__ __forceinline__ int causal_first_qtile(const BwdArgs& a, int s0, int Tb) {
+  if (!a.causal) return 0;
+  const int x = s0 - (a.S - a.T) - Tb + 1;  // need qt*Tb + Tb - 1 + (S - T) >= s0
+  return x <= 0 ? 0 : (x + Tb - 1) / Tb;
+}
+
+// One past the last KV tile (of kvr keys) the causal mask lets the rows
+// [t0, min(t0 + Tb, T)) see.
+__device__ __forceinline__ int causal_kv_end(const BwdArgs& a, int t0, int Tb, int kvr) {
+  if (!a.causal) return a.n_kvtiles;
+  const int lim = min(t0 + Tb, a.T) - 1 + (a.S - a.T);
+  return lim < 0 ? 0 : min(a.n_kvtiles, lim / kvr + 1);
+}
+
+// Apply the causal / segment / key-range mask to 32 consecutive key columns
+// [scol, scol + 32) of the row at position t.
 __device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int t, int my_seg,
                                        int scol) {
-  if (a.causal) {
+  const int off = a.S - a.T;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (scol + i > t) s[i] = -INFINITY;
+  for (int i = 0; i < 32; ++i) {
+    const int sc = scol + i;
+    if (sc >= a.S || (a.causal && sc > t + off)) s[i] = -INFINITY;
   }
   if (a.seg_q != nullptr) {
-    const int4* kid = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + scol);
+    const int32_t* ids = a.seg_kv + (long)b * a.S + scol;
+    if ((a.S & 3) == 0 && scol + 32 <= a.S) {  // 16-byte aligned, in range: vector loads
+      const int4* kid = reinterpret_cast<const int4*>(ids);
 #pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4) {
-      const int4 v = __ldg(kid + i4);
-      if (v.x != my_seg) s[4 * i4 + 0] = -INFINITY;
-      if (v.y != my_seg) s[4 * i4 + 1] = -INFINITY;
-      if (v.z != my_seg) s[4 * i4 + 2] = -INFINITY;
-      if (v.w != my_seg) s[4 * i4 + 3] = -INFINITY;
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const int4 v = __ldg(kid + i4);
+        if (v.x != my_seg) s[4 * i4 + 0] = -INFINITY;
+        if (v.y != my_seg) s[4 * i4 + 1] = -INFINITY;
+        if (v.z != my_seg) s[4 * i4 + 2] = -INFINITY;
+        if (v.w != my_seg) s[4 * i4 + 3] = -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (scol + i < a.S && __ldg(ids + i) != my_seg) s[i] = -INFINITY;
     }
   }
 }
@@ -130,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
   // qr/kr are only read when segment ids are given (they live past D).
-  int jt_end = a.n_kvtiles;
-  if (a.causal) jt_end = min(a.n_kvtiles, (t0 + Tb - 1) / BN + 1);
+  const int jt_end = causal_kv_end(a, t0, Tb, BN);
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -296,12 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   } else {
     // softmax-side: thread r owns packed query row r
     const int r = tid, g = r / Tb, t = t0 + (r - g * Tb);
+    const bool valid = t < a.T;  // rows past T (ragged last tile) are inert
     const long row = ((long)bk * a.G + g) * a.T + t;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float lse = a.lse[row];
+    const float lse = valid ? a.lse[row] : -INFINITY;
     const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-    const float Dr = a.delta[row];
-    const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
+    const float Dr = valid ? a.delta[row] : 0.f;
+    const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
     bool ok = true;
     int n = 0;
     for (int jt = 0; jt < jt_end; ++jt) {
@@ -422,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   const int s0 = jt * BN;
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
-  const int qt_begin = a.causal ? s0 / Tb : 0;
+  const int qt_begin = causal_first_qtile(a, s0, Tb);
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -546,11 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const int cls = tile_class(a, qr, kr, b, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int g = r / Tb, t = qt * Tb + (r - g * Tb);
+      const bool valid = t < a.T;  // rows past T (ragged last tile) are inert
       const long row = ((long)bk * a.G + g) * a.T + t;
-      const float lse = a.lse[row];
+      const float lse = valid ? a.lse[row] : -INFINITY;
       const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-      const float Dr = a.delta[row];
-      const int my_seg = a.seg_q ? a.seg_q[(long)b * a.T + t] : 0;
+      const float Dr = valid ? a.delta[row] : 0.f;
+      const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
       if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
       // P and dS shared buffers are free once the previous tile's dV^T and dK^T
       // are done (the last half's release barriers follow every earlier product).
@@ -614,8 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         }
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
-          dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+          if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
+            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
+            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+          }
         }
       }
     }
@@ -661,8 +693,9 @@ __global__ void seg_ranges_kernel(const int32_t* __restrict__ seg, int L, int ti
   const long b = w / n_tiles;
   const int j = (int)(w - b * n_tiles);
   const int32_t* p = seg + b * L + (long)j * tile;
+  const int n = min(tile, L - j * tile);  // the last tile may be ragged
   int mn = INT_MAX, mx = INT_MIN;
-  for (int i = lane; i < tile; i += 32) {
+  for (int i = lane; i < n; i += 32) {
     const int v = __ldg(p + i);
     mn = min(mn, v);
     mx = max(mx, v);
@@ -704,7 +737,8 @@ cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
 
 size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
   const size_t d = ((size_t)B * K * G * T * sizeof(float) + 255) & ~(size_t)255;
-  const size_t nq = (size_t)T / (kRows / G), nk = (size_t)S / bwd_kv_rows(H);
+  const size_t tb = kRows / G, kvr = bwd_kv_rows(H);
+  const size_t nq = (T + tb - 1) / tb, nk = (S + kvr - 1) / kvr;
   const size_t r = ((size_t)B * (nq + nk) * sizeof(int2) + 255) & ~(size_t)255;
   return d + r;
 }

@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int bk = blockIdx.y;
   const int b = bk / a.K;
   const int t0 = qt * Tb;
-  const int n_kv_all = a.S / kKvRows;
+  const int n_valid = min(Tb, a.T - t0);   // positions of this tile below T
+  const int off = a.S - a.T;               // causal keeps s <= t + off
+  const int n_kv_all = (a.S + kKvRows - 1) / kKvRows;
   const bool segs = a.seg_q != nullptr;
 
   // ---------------------------------------------------------------- setup
@@ -133,14 +135,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     prefetch_tmap(&a.tm_v);
   }
 
-  // KV tiles the causal mask can reach: keys s <= t_max.
+  // KV tiles the causal mask can reach: keys s <= t_last + off.
   int n_kv = n_kv_all;
-  if (a.causal) n_kv = min(n_kv_all, (t0 + Tb - 1) / kKvRows + 1);
+  if (a.causal) {
+    const int lim = t0 + n_valid - 1 + off;
+    n_kv = lim < 0 ? 0 : min(n_kv_all, lim / kKvRows + 1);
+  }
 
   // Segment range of this Q tile (ids of its Tb positions).
   if (segs && warp == 0) {
     int mn = INT_MAX, mx = INT_MIN;
-    for (int i = lane; i < Tb; i += 32) {
+    for (int i = lane; i < n_valid; i += 32) {
       int v = a.seg_q[(long)b * a.T + t0 + i];
       mn = min(mn, v);
       mx = max(mx, v);
@@ -154,11 +159,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // Classify every reachable KV tile (lazy mask: only per-tile id ranges).
   for (int j = warp; j < n_kv; j += kThreads / 32) {
     uint8_t c = TILE_FULL;
-    if (a.causal && (j + 1) * kKvRows - 1 > t0) c = TILE_PARTIAL;  // crosses the diagonal
+    const int s_last = min((j + 1) * kKvRows, a.S) - 1;
+    if (a.causal && s_last > t0 + off) c = TILE_PARTIAL;  // crosses the diagonal
+    if ((j + 1) * kKvRows > a.S) c = TILE_PARTIAL;         // ragged last tile
     if (segs) {
-      const int4 v = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + j * kKvRows)[lane];
-      int mn = min(min(v.x, v.y), min(v.z, v.w));
-      int mx = max(max(v.x, v.y), max(v.z, v.w));
+      int mn = INT_MAX, mx = INT_MIN;
+      for (int e = 0; e < 4; ++e) {
+        const int sk = j * kKvRows + lane * 4 + e;
+        if (sk < a.S) {
+          const int v = a.seg_kv[(long)b * a.S + sk];
+          mn = min(mn, v);
+          mx = max(mx, v);
+        }
+      }
       mn = __reduce_min_sync(0xffffffffu, mn);
       mx = __reduce_max_sync(0xffffffffu, mx);
       const int qmn = qrange[0], qmx = qrange[1];
@@ -286,8 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     const int r = tid;  // TMEM lane == packed row
     const int g = r / Tb;
     const int t = t0 + (r - g * Tb);
+    const bool valid = t < a.T;  // rows past T (ragged last tile) are computed, not stored
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int my_seg = segs ? a.seg_q[(long)b * a.T + t] : 0;
+    const int my_seg = (segs && valid) ? a.seg_q[(long)b * a.T + t] : 0;
     float m_ref = -INFINITY;  // running max, log2 units
     float l = 0.f;            // running denominator (relative to m_ref)
     bool ok = true;
@@ -304,21 +318,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       float* s = reinterpret_cast<float*>(&sv[0][0]);
       if (partial) {
         const int s0 = j * kKvRows;
-        if (a.causal) {
+        const int lim = a.causal ? min(t + off, a.S - 1) : a.S - 1;  // last key kept
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (s0 + c > t) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (s0 + c > lim) s[c] = -INFINITY;
         if (segs) {
           // every thread reads the same 512 B of key ids: served by L1 broadcast
-          const int4* kid = reinterpret_cast<const int4*>(a.seg_kv + (long)b * a.S + s0);
+          const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
+          if ((a.S & 3) == 0 && s0 + 128 <= a.S) {  // aligned and in range
+            const int4* kid = reinterpret_cast<const int4*>(ids);
 #pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
-            const int4 v = __ldg(kid + c4);
-            if (v.x != my_seg) s[4 * c4 + 0] = -INFINITY;
-            if (v.y != my_seg) s[4 * c4 + 1] = -INFINITY;
-            if (v.z != my_seg) s[4 * c4 + 2] = -INFINITY;
-            if (v.w != my_seg) s[4 * c4 + 3] = -INFINITY;
+            for (int c4 = 0; c4 < 32; ++c4) {
+              const int4 v = __ldg(kid + c4);
+              if (v.x != my_seg) s[4 * c4 + 0] = -INFINITY;
+              if (v.y != my_seg) s[4 * c4 + 1] = -INFINITY;
+              if (v.z != my_seg) s[4 * c4 + 2] = -INFINITY;
+              if (v.w != my_seg) s[4 * c4 + 3] = -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (s0 + c < a.S && __ldg(ids + c) != my_seg) s[c] = -INFINITY;
           }
         }
       }
@@ -407,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
       for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
     }
-    a.lse[row] = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    if (valid) a.lse[row] = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     fence_proxy_async_smem();
     named_bar_sync(1, kRows);
     if (tid == 0) {

@@ -38,8 +38,7 @@ enum {
   FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, one seg pointer without the
                                  other, misaligned pointer, workspace too small */
   FA_ERR_UNSUPPORTED = 2,     /* H not in {64,128,256}, G not a power of two <= 128,
-                                 T or S not a multiple of 128, causal with T != S,
-                                 backward with H == 64 */
+                                 S > 131072, B*K > 65535, backward with H == 64 */
   FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device wait ran out (kernel gave up) */
 };
@@ -48,8 +47,10 @@ enum {
  * Forward pass: for every (b, k, g, t)
  *   o[b,k,g,t,:]  = sum_s softmax_s(L)[s] * v[b,k,s,:],  L[s] = q[b,k,g,t,:] . k[b,k,s,:]
  *   lse[b,k,g,t]  = log sum_s exp(L[s])
- * over the keys kept by the mask: s <= t when `causal` (same absolute index for
- * queries and keys), and seg_q[b,t] == seg_kv[b,s] when segment ids are given
+ * over the keys kept by the mask: s <= t + (S - T) when `causal` (queries are
+ * aligned to the end of the keys: for T == S this is s <= t, and the last
+ * query always sees every key), and seg_q[b,t] == seg_kv[b,s] when segment ids
+ * are given
  * (SegmentIds, jax_flash_attn_tpu docs: only tokens with the same id attend).
  * This is the online-softmax sweep of "Chunked attention" / "Optimizing the
  * kernel" (running max m, denominator, rescaled accumulator, output divided
@@ -58,7 +59,8 @@ enum {
  * written to memory and no mask array exists: masks are generated per tile
  * and tiles the mask removes entirely are skipped (axlearn PR "Optimize TPU
  * Flash Attention", lazy causal mask).
- * T == 0 or S == 0 or B*K == 0: no kernel work beyond filling o = 0, lse = -inf.
+ * T and S are arbitrary (no multiple-of-128 requirement; T = 1 is a decode
+ * step).  T == 0 or B*K == 0: nothing to do; S == 0: o = 0, lse = -inf.
  */
 int fa_fwd(const void* q, const void* k, const void* v,
            const int32_t* seg_q, const int32_t* seg_kv, int causal,

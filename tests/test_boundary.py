@@ -48,7 +48,9 @@ def test_workspace_size(clib):
     assert n % 256 == 0
     assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256
     assert binding.fa_bwd_workspace_size(0, 1, 1, 128, 128, 128) == 0
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 128) == 0   # unsupported
+    # ragged sizes: D rows rounded up to 256 B, then one range pair per tile
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 96) == 0      # H unsupported
 
 
 def _fwd(clib, *, q=16, k=16, v=16, sq=None, skv=None, causal=0, o=16, lse=16,
@@ -59,6 +61,8 @@ def _fwd(clib, *, q=16, k=16, v=16, sq=None, skv=None, causal=0, o=16, lse=16,
 
 
 def test_fwd_validation(clib):
+    # every call below is rejected (or has nothing to do) before any launch:
+    # the pointers are fake
     assert _fwd(clib, q=0) == binding.FA_ERR_INVALID_ARG
     assert _fwd(clib, q=8) == binding.FA_ERR_INVALID_ARG            # misaligned
     assert _fwd(clib, sq=16) == binding.FA_ERR_INVALID_ARG           # one seg pointer
@@ -66,8 +70,6 @@ def test_fwd_validation(clib):
     assert _fwd(clib, H=96) == binding.FA_ERR_UNSUPPORTED
     assert _fwd(clib, G=3) == binding.FA_ERR_UNSUPPORTED
     assert _fwd(clib, G=256) == binding.FA_ERR_UNSUPPORTED
-    assert _fwd(clib, T=100, S=100) == binding.FA_ERR_UNSUPPORTED
-    assert _fwd(clib, causal=1, T=128, S=256) == binding.FA_ERR_UNSUPPORTED
     assert _fwd(clib, S=256 * 1024) == binding.FA_ERR_UNSUPPORTED
     assert _fwd(clib, T=0) == binding.FA_OK                          # nothing to do
 

@@ -74,6 +74,28 @@ def test_fully_masked_rows_get_zero_gradient():
     assert torch.all(dq[0, 0, :, 100:140] == 0)
 
 
+@pytest.mark.parametrize("T,S", [(300, 300), (77, 77), (1000, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,G", [(128, 4), (256, 8)])
+def test_ragged_lengths(T, S, causal, H, G):
+    run_case(1, 2, G, T, S, H, causal=causal, seed=T + H)
+
+
+@pytest.mark.parametrize("T,S", [(100, 300), (300, 100), (1, 500), (5, 3)])
+@pytest.mark.parametrize("H", [128, 256])
+def test_rectangular_causal(T, S, H):
+    run_case(2, 1, 4, T, S, H, causal=True, seed=T + S)
+
+
+def test_ragged_segments():
+    T = 333
+    seg = inputs.document_segment_ids(2, T, seed=5, lo=40, hi=200)
+    run_case(2, 2, 4, T, T, 128, causal=True, seg_q=seg, seg_kv=seg, seed=7)
+    seg_q = inputs.random_segment_ids(1, T, 3, seed=3)
+    seg_kv = inputs.random_segment_ids(1, T + 5, 3, seed=4)
+    run_case(1, 1, 8, T, T + 5, 256, causal=False, seg_q=seg_q, seg_kv=seg_kv, seed=8)
+
+
 def test_causal_workload_h128_t1024_full():
     w = inputs.WORKLOADS["gqa_causal_h128_t1024"]
     run_case(w.B, w.K, w.G, w.T, w.S, w.H, causal=True, seed=w.seed)

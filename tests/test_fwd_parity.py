@@ -94,6 +94,30 @@ def test_large_logits_are_stable():
     check_lse(lse.cpu().numpy().astype(np.float64), l_ref)
 
 
+@pytest.mark.parametrize("T,S", [(300, 300), (200, 200), (1000, 1000), (77, 77)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,G", [(64, 4), (128, 8), (256, 1)])
+def test_ragged_lengths(T, S, causal, H, G):
+    run_case(1, 2, G, T, S, H, causal=causal, seed=T + H + G)
+
+
+@pytest.mark.parametrize("T,S", [(100, 300), (300, 100), (128, 1000), (1, 1000), (1, 1), (5, 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_and_decode_shapes(T, S, causal):
+    # causal with T != S keeps s <= t + (S - T); T = 1 is a decode step
+    run_case(2, 2, 8, T, S, 128, causal=causal, seed=T * 7 + S)
+
+
+@pytest.mark.parametrize("T", [333, 1001])
+def test_ragged_segments(T):
+    # T not a multiple of 4: segment-id rows are not 16-byte aligned
+    seg = inputs.document_segment_ids(2, T, seed=T, lo=40, hi=200)
+    run_case(2, 2, 4, T, T, 128, causal=True, seg_q=seg, seg_kv=seg, seed=T)
+    seg_q = inputs.random_segment_ids(1, T, 3, seed=1)
+    seg_kv = inputs.random_segment_ids(1, T + 5, 3, seed=2)
+    run_case(1, 1, 8, T, T + 5, 256, causal=False, seg_q=seg_q, seg_kv=seg_kv, seed=T + 1)
+
+
 def test_causal_workload_h128_t1024_full():
     w = inputs.WORKLOADS["gqa_causal_h128_t1024"]
     run_case(w.B, w.K, w.G, w.T, w.S, w.H, causal=True, seed=w.seed)
