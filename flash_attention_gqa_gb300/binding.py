@@ -28,6 +28,10 @@ _I = ctypes.c_int
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "fa_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "fa_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _P, ctypes.c_size_t,
+                            _I, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_splitkv_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_fwd_splitkv_default_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, ctypes.c_size_t,
                     _I, _I, _I, _I, _I, _I, _P]),
     "fa_bwd_stage": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
@@ -104,6 +108,27 @@ def fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, stream=None, check=True) -> i
     return rc
 
 
+def fa_fwd_splitkv(q, k, v, seg_q, seg_kv, causal, o, lse, n_splits, workspace, stream=None,
+                   check=True) -> int:
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(seg_q), _ptr(seg_kv),
+                               int(bool(causal)), _ptr(o), _ptr(lse), int(n_splits),
+                               _ptr(workspace), ws_bytes, B, K, G, T, S, H, _stream(stream))
+    if check:
+        _check("fa_fwd_splitkv", rc)
+    return rc
+
+
+def fa_fwd_splitkv_workspace_size(B, K, G, T, S, H, n_splits) -> int:
+    return int(load().fa_fwd_splitkv_workspace_size(B, K, G, T, S, H, n_splits))
+
+
+def fa_fwd_splitkv_default_splits(B, K, G, T, S, H) -> int:
+    return int(load().fa_fwd_splitkv_default_splits(B, K, G, T, S, H))
+
+
 def fa_bwd_workspace_size(B, K, G, T, S, H) -> int:
     return int(load().fa_bwd_workspace_size(B, K, G, T, S, H))
 
@@ -173,6 +198,21 @@ def attention_forward(q, k, v, *, causal=False, seg_q=None, seg_kv=None, stream=
     o = torch.empty_like(q)
     lse = torch.empty((B, K, G, T), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, stream)
+    return o, lse
+
+
+def attention_forward_splitkv(q, k, v, *, causal=False, seg_q=None, seg_kv=None, n_splits=None,
+                              stream=None):
+    """fa_fwd_splitkv with torch-allocated outputs and workspace."""
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    if n_splits is None:
+        n_splits = fa_fwd_splitkv_default_splits(B, K, G, T, S, H)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, K, G, T), dtype=torch.float32, device=q.device)
+    n = fa_fwd_splitkv_workspace_size(B, K, G, T, S, H, n_splits)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    fa_fwd_splitkv(q, k, v, seg_q, seg_kv, causal, o, lse, n_splits, ws, stream)
     return o, lse
 
 

@@ -143,10 +143,85 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
   a.causal = causal ? 1 : 0;
   a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
+  a.n_splits = 1;
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
   return fa::launch_fwd(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+namespace {
+size_t splitkv_parts(int B, int K, int G, int T, int H, int n_splits, size_t* o_bytes) {
+  const size_t rows = (size_t)B * K * G * T;
+  const size_t ob = ((size_t)n_splits * rows * H * sizeof(float) + 255) & ~(size_t)255;
+  const size_t lb = ((size_t)n_splits * rows * sizeof(float) + 255) & ~(size_t)255;
+  if (o_bytes) *o_bytes = ob;
+  return ob + lb;
+}
+}  // namespace
+
+size_t fa_fwd_splitkv_workspace_size(int B, int K, int G, int T, int S, int H, int n_splits) {
+  if (B <= 0 || K <= 0 || G <= 0 || T <= 0 || S < 0 || n_splits < 1 || n_splits > 256) return 0;
+  if (check_shapes(B, K, G, T, S, H, 0, nullptr, nullptr) != FA_OK) return 0;
+  return splitkv_parts(B, K, G, T, H, n_splits, nullptr);
+}
+
+int fa_fwd_splitkv_default_splits(int B, int K, int G, int T, int S, int H) {
+  if (B <= 0 || K <= 0 || G <= 0 || T <= 0 || S <= 0) return 1;
+  if (check_shapes(B, K, G, T, S, H, 0, nullptr, nullptr) != FA_OK) return 1;
+  const long ctas = (long)((T + kRows / G - 1) / (kRows / G)) * B * K;
+  const int sms = fa_device_sm_count();
+  const int kv_tiles = (S + fa::kKvRows - 1) / fa::kKvRows;
+  // Splitting costs partial writes and a merge: only worth it when the Q
+  // tiles alone leave SMs idle.
+  long n = (sms > 0 && ctas < sms) ? (2L * sms + ctas - 1) / ctas : 1;
+  n = n < 1 ? 1 : n;
+  n = n > kv_tiles ? kv_tiles : n;
+  return (int)(n > 64 ? 64 : n);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int32_t* seg_q,
+                   const int32_t* seg_kv, int causal, void* o, float* lse, int n_splits,
+                   void* workspace, size_t workspace_bytes, int B, int K, int G, int T, int S, int H,
+                   void* stream) {
+  if (n_splits < 1 || n_splits > 256) return FA_ERR_INVALID_ARG;
+  if (n_splits == 1)
+    return fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, B, K, G, T, S, H, stream);
+  const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
+  if (rc != FA_OK) return rc;
+  const long rows = (long)B * K * G * T;
+  const bool has_kv = (long)B * K * S > 0;
+  if (rows > 0 && (!q || !o || !lse || !aligned16(q) || !aligned16(o) ||
+                   (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return FA_ERR_INVALID_ARG;
+  if (has_kv && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+  if (rows == 0 || S == 0) return fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, B, K, G, T, S, H, stream);
+  size_t o_bytes = 0;
+  const size_t need = splitkv_parts(B, K, G, T, H, n_splits, &o_bytes);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  fa::FwdArgs a{};
+  const int BK = B * K;
+  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
+      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows) || !make_q_map(&a.tm_o, o, BK, G, T, H))
+    return FA_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.seg_q = seg_q;
+  a.seg_kv = seg_kv;
+  a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
+  a.causal = causal ? 1 : 0;
+  a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
+  a.n_splits = n_splits;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  a.err = error_word();
+  a.wait_limit_ns = wait_limit();
+  if (!a.err) return FA_ERR_CUDA;
+  cudaError_t e = fa::launch_fwd(a, st);
+  if (e == cudaSuccess) e = fa::launch_split_combine(a.part_o, a.part_lse, n_splits, o, lse, rows, H, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {

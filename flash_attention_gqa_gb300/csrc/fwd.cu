@@ -200,7 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tiles = *n_tiles_s;
+  // Split-KV mode: this CTA takes slice blockIdx.z of the schedule.
+  const int n_sched = *n_tiles_s;
+  const int per_split = (n_sched + a.n_splits - 1) / a.n_splits;
+  const int sched_begin = min(n_sched, (int)blockIdx.z * per_split);
+  const int n_tiles = min(n_sched, sched_begin + per_split) - sched_begin;
+  const uint16_t* sched = tiles + sched_begin;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         else if (u == 2 * n_tiles - 1) { is_k = false; n = n_tiles - 1; }
         else if (u & 1) { is_k = true; n = (u + 1) / 2; }
         else { is_k = false; n = u / 2 - 1; }
-        const int j = tiles[n] & 0x7fff;
+        const int j = sched[n] & 0x7fff;
         const CUtensorMap* m = is_k ? &a.tm_k : &a.tm_v;
         for (int c = 0; c < HC; ++c, ++seq) {
           const int slot = seq % kSlots;
@@ -306,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     float l = 0.f;            // running denominator (relative to m_ref)
     bool ok = true;
     for (int n = 0; n < n_tiles; ++n) {
-      const int j = tiles[n] & 0x7fff;
-      const bool partial = (tiles[n] & 0x8000) != 0;
+      const int j = sched[n] & 0x7fff;
+      const bool partial = (sched[n] & 0x8000) != 0;
       if (!warp_wait(bars.s_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_col = 256 + 128 * (n & 1);
@@ -407,34 +412,61 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                       warp_wait(bars.pv_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, ab);
     if (have) tc_fence_after();
     const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+    const float lse_row = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    if (a.n_splits > 1) {
+      // Split-KV: this split's normalised partial output (fp32) and lse; the
+      // combine kernel merges the splits with weights exp(lse_i - lse).
+      const long prow = (long)blockIdx.z * ((long)a.B * a.K * a.G * a.T) + row;
+      float* dst = a.part_o + prow * H;
 #pragma unroll 1
-    for (int c = 0; c < H; c += 32) {
-      uint32_t ov[32];
-      if (have) {
-        tmem_ld32(tmem + lane_base + c, ov);
-        tmem_wait_ld();
-      } else {
+      for (int c = 0; c < H; c += 32) {
+        uint32_t ov[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + c, ov);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = 0;
+          for (int i = 0; i < 32; ++i) ov[i] = 0;
+        }
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dst + c)[i] =
+                make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                            __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+        }
       }
-      uint4 pkd[4];
-      uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+      if (valid) a.part_lse[prow] = lse_row;
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < H; c += 32) {
+        uint32_t ov[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + c, ov);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-      uint8_t* chunk = sm + L::q_off + (c / 64) * kChunkBytes;
-      const uint32_t u0 = (c % 64) / 8;
+          for (int i = 0; i < 32; ++i) ov[i] = 0;
+        }
+        uint4 pkd[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
-    }
-    if (valid) a.lse[row] = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-    fence_proxy_async_smem();
-    named_bar_sync(1, kRows);
-    if (tid == 0) {
-      for (int c = 0; c < HC; ++c)
-        tma_store_4d(&a.tm_o, sbase + L::q_off + c * kChunkBytes, c * 64, t0, 0, bk);
-      bulk_commit();
-      bulk_wait_read0();
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+        uint8_t* chunk = sm + L::q_off + (c / 64) * kChunkBytes;
+        const uint32_t u0 = (c % 64) / 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
+      }
+      if (valid) a.lse[row] = lse_row;
+      fence_proxy_async_smem();
+      named_bar_sync(1, kRows);
+      if (tid == 0) {
+        for (int c = 0; c < HC; ++c)
+          tma_store_4d(&a.tm_o, sbase + L::q_off + c * kChunkBytes, c * 64, t0, 0, bk);
+        bulk_commit();
+        bulk_wait_read0();
+      }
     }
   }
 
@@ -479,12 +511,65 @@ cudaError_t launch_fwd_h(const FwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(a.n_qtiles, a.B * a.K);
+  dim3 grid(a.n_qtiles, a.B * a.K, a.n_splits);
   fa_fwd_kernel<H><<<grid, kThreads, L::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
+// Merge split-KV partial results: one warp per query row.
+//   lse = log sum_i exp(lse_i),  o = sum_i exp(lse_i - lse) * o_i
+template <int H>
+__global__ void split_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                     int n_splits, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                     long rows) {
+  const long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int i = 0; i < n_splits; ++i) m = fmaxf(m, __ldg(part_lse + (long)i * rows + row));
+  constexpr int PER = H / 32;  // columns per lane
+  float acc[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+  float sum = 0.f;
+  if (m != -INFINITY) {
+    for (int i = 0; i < n_splits; ++i) {
+      const float li = __ldg(part_lse + (long)i * rows + row);
+      if (li == -INFINITY) continue;
+      const float w = __expf(li - m);
+      sum += w;
+      const float* src = part_o + ((long)i * rows + row) * H + lane * PER;
+#pragma unroll
+      for (int j = 0; j < PER; j += 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(src + j));
+        acc[j] = fmaf(w, v.x, acc[j]);
+        acc[j + 1] = fmaf(w, v.y, acc[j + 1]);
+      }
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  __nv_bfloat16* dst = o + row * H + lane * PER;
+#pragma unroll
+  for (int j = 0; j < PER; j += 2)
+    *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16x2(acc[j] * inv, acc[j + 1] * inv);
+  if (lane == 0) lse[row] = sum > 0.f ? m + __logf(sum) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int n_splits, void* o,
+                                 float* lse, long rows, int H, cudaStream_t st) {
+  const int warps = 8;
+  const unsigned blocks = (unsigned)((rows + warps - 1) / warps);
+  auto* ob = reinterpret_cast<__nv_bfloat16*>(o);
+  switch (H) {
+    case 64: split_combine_kernel<64><<<blocks, warps * 32, 0, st>>>(part_o, part_lse, n_splits, ob, lse, rows); break;
+    case 128: split_combine_kernel<128><<<blocks, warps * 32, 0, st>>>(part_o, part_lse, n_splits, ob, lse, rows); break;
+    case 256: split_combine_kernel<256><<<blocks, warps * 32, 0, st>>>(part_o, part_lse, n_splits, ob, lse, rows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
   switch (a.H) {

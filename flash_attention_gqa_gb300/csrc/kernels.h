@@ -22,7 +22,10 @@ struct FwdArgs {
   const int32_t* seg_kv;  // [B, S] or null
   int B, K, G, T, S, H;
   int causal;
-  int n_qtiles;       // T / (128 / G)
+  int n_qtiles;       // ceil(T / (128 / G))
+  int n_splits;       // > 1: split-KV mode (grid.z splits the KV-tile schedule)
+  float* part_o;      // split-KV: fp32 [n_splits, B*K*G*T, H] partial outputs
+  float* part_lse;    // split-KV: [n_splits, B*K*G*T] partial lse (natural log)
   uint32_t* err;      // device error word
   uint64_t wait_limit_ns;
 };
@@ -55,6 +58,8 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_fill_empty(void* o, float* lse, long rows, int H, cudaStream_t st);
+cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int n_splits, void* o,
+                                 float* lse, long rows, int H, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 // KV rows per tile of the backward kernels for a head dim.

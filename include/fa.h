@@ -67,6 +67,31 @@ int fa_fwd(const void* q, const void* k, const void* v,
            void* o, float* lse,
            int B, int K, int G, int T, int S, int H, void* stream);
 
+/*
+ * Split-KV forward, for few query rows per kv head (decode, T = 1, or small
+ * T): the same result as fa_fwd, with every Q tile's KV-tile schedule cut
+ * into n_splits contiguous slices processed by separate CTAs.  Each slice
+ * writes its normalised partial output (fp32) and partial lse into
+ * `workspace`; a second kernel merges them, o = sum_i exp(lse_i - lse) o_i
+ * with lse = log sum_i exp(lse_i).  Not on the pages (their inference note
+ * only observes that decode is memory-bound); this keeps every SM streaming
+ * K and V.  n_splits in [1, 256]; 1 is fa_fwd.  `workspace` (256-byte
+ * aligned) must hold fa_fwd_splitkv_workspace_size(...) bytes.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v,
+                   const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                   void* o, float* lse, int n_splits,
+                   void* workspace, size_t workspace_bytes,
+                   int B, int K, int G, int T, int S, int H, void* stream);
+
+/* Workspace bytes of fa_fwd_splitkv (0 for unsupported sizes or n_splits). */
+size_t fa_fwd_splitkv_workspace_size(int B, int K, int G, int T, int S, int H, int n_splits);
+
+/* A split count that gives about two CTAs per SM of the current device when
+   the Q tiles alone number fewer CTAs than SMs (1 otherwise); at most 64 and
+   at most the number of KV tiles. */
+int fa_fwd_splitkv_default_splits(int B, int K, int G, int T, int S, int H);
+
 /* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256;
    0 for empty or unsupported sizes). */
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);

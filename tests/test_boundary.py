@@ -88,6 +88,19 @@ def test_bwd_validation(clib):
     assert call(H=64) == binding.FA_ERR_UNSUPPORTED
 
 
+def test_splitkv_host_side(clib):
+    assert binding.fa_fwd_splitkv_workspace_size(1, 2, 8, 1, 4096, 128, 4) == \
+        ((4 * 16 * 128 * 4 + 255) // 256) * 256 + 256
+    assert binding.fa_fwd_splitkv_workspace_size(1, 2, 8, 1, 4096, 128, 0) == 0
+    P = ctypes.c_void_p
+    rc = clib.fa_fwd_splitkv(P(16), P(16), P(16), None, None, 0, P(16), P(16), 0, P(256), 1 << 20,
+                             1, 1, 8, 1, 256, 128, None)
+    assert rc == binding.FA_ERR_INVALID_ARG          # n_splits must be >= 1
+    rc = clib.fa_fwd_splitkv(P(16), P(16), P(16), None, None, 0, P(16), P(16), 4, P(256), 16,
+                             1, 1, 8, 1, 256, 128, None)
+    assert rc == binding.FA_ERR_INVALID_ARG          # workspace too small
+
+
 def test_wait_limit_setter(clib):
     assert binding.fa_set_wait_limit_ns(0) == binding.FA_ERR_INVALID_ARG
     assert binding.fa_set_wait_limit_ns(2_000_000_000) == binding.FA_OK

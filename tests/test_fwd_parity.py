@@ -148,3 +148,47 @@ def test_repeatable():
     o1, l1 = binding.attention_forward(q, k, v, causal=True)
     o2, l2 = binding.attention_forward(q, k, v, causal=True)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------- split-KV
+
+def run_split(B, K, G, T, S, H, n_splits, causal=False, seg_q=None, seg_kv=None, seed=0):
+    x = inputs.make_tensors(B, K, G, T, S, H, seed=seed, backward=False, seg_q=seg_q,
+                            seg_kv=seg_kv)
+    dev = torch.device("cuda")
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    sq = None if x.seg_q is None else x.seg_q.to(dev)
+    skv = None if x.seg_kv is None else x.seg_kv.to(dev)
+    o, lse = binding.attention_forward_splitkv(q, k, v, causal=causal, seg_q=sq, seg_kv=skv,
+                                               n_splits=n_splits)
+    assert binding.fa_check_status() == binding.FA_OK
+    o_ref, l_ref = oracle.attention_forward(x.q, x.k, x.v, causal=causal, seg_q=x.seg_q,
+                                            seg_kv=x.seg_kv)
+    check_o(to_np(o), o_ref)
+    check_lse(lse.cpu().numpy().astype(np.float64), l_ref)
+
+
+@pytest.mark.parametrize("H", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n_splits", [2, 7, 40])
+def test_splitkv_decode(H, causal, n_splits):
+    run_split(2, 2, 8, 1, 3000, H, n_splits, causal=causal, seed=H + n_splits)
+
+
+@pytest.mark.parametrize("T,S", [(16, 4096), (100, 1000), (300, 300)])
+def test_splitkv_small_t(T, S):
+    run_split(1, 2, 4, T, S, 128, 5, causal=True, seed=T)
+
+
+def test_splitkv_segments_and_more_splits_than_tiles():
+    T = 200
+    seg = inputs.document_segment_ids(2, T, seed=2, lo=20, hi=90)
+    run_split(2, 1, 4, T, T, 128, 3, causal=True, seg_q=seg, seg_kv=seg, seed=4)
+    run_split(1, 1, 8, 1, 300, 128, 9, causal=False, seed=5)   # 9 splits, 3 kv tiles
+
+
+def test_splitkv_default_splits():
+    n = binding.fa_fwd_splitkv_default_splits(1, 8, 8, 1, 32768, 128)
+    assert 1 <= n <= 64
+    assert binding.fa_fwd_splitkv_default_splits(1, 2, 8, 8192, 8192, 256) == 1
+    run_split(1, 8, 8, 1, 8192, 128, None, causal=True, seed=6)
