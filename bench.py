@@ -41,10 +41,10 @@ L2_BYTES = 129 * 2**20
 # DRAM traffic per launch of the roofline kernel from one ncu capture, keyed
 # by kernel name; valid only while the kernel source hashes to `src_sha`.
 NCU_TRAFFIC = {
-    # profiles/kernels_gqa_causal_h256_t8192.md (ncu --set full, one launch each)
-    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 174813952, "src_sha": "929d0165f0a9896f"},
-    "fa_bwd_dq_kernel": {"bytes_per_launch": 188100608, "src_sha": "929d0165f0a9896f"},
-    "fa_fwd_kernel": {"bytes_per_launch": 107298304, "src_sha": "86eb98f27f267b2b"},
+    # profiles/kernels_gqa_causal_h256_t8192.md (one launch each, --metrics capture)
+    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 173891584, "src_sha": "bdbd9c8010708aaa"},
+    "fa_bwd_dq_kernel": {"bytes_per_launch": 188659456, "src_sha": "bdbd9c8010708aaa"},
+    "fa_fwd_kernel": {"bytes_per_launch": 112082176, "src_sha": "a4993dded1c934a9"},
 }
 
 
