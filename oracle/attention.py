@@ -28,6 +28,11 @@ Readings where the pages are silent (all listed with the design notes):
   * causal keeps s <= t + (S - T): queries are aligned to the end of the keys,
     so the last query sees every key; for T == S this is s <= t with the same
     absolute index for queries and keys (the pages only use T == S);
+  * an optional explicit mask ``mask[h, t, s]`` (h = k*G + g, the query head
+    within a batch row, or a single head shared by all) is ANDed with the causal and segment
+    masks: the dense form of the block-sparse mask metadata the kernels take
+    (splash attention's MultiHeadMask / process_mask in the tutorial's
+    "Our first kernel" baseline);
   * a query row with no kept key has O = 0, lse = -inf and contributes no
     gradient ("only the same id can attend" leaves it nothing to attend to);
   * natural exp/log throughout; lse is in natural-log units.
@@ -101,9 +106,19 @@ def _key_range(t1: int, S: int, causal: bool, offset: int = 0) -> int:
     return max(0, min(S, t1 + offset)) if causal else S
 
 
+def _head_mask(mask, kh, G, t_idx, s_idx):
+    """[G, rows, keys] slice of the explicit mask for kv head kh (or None)."""
+    if mask is None:
+        return None
+    m = np.asarray(mask, dtype=bool)
+    if m.shape[0] == 1:
+        return np.broadcast_to(m[0][np.ix_(t_idx, s_idx)][None], (G, len(t_idx), len(s_idx)))
+    return np.stack([m[kh * G + g][np.ix_(t_idx, s_idx)] for g in range(G)])
+
+
 def attention_forward(q, k, v, *, causal: bool = False, seg_q=None,
                       seg_kv=None, row_block: int = 512,
-                      heads: Optional[Sequence[tuple]] = None):
+                      heads: Optional[Sequence[tuple]] = None, mask=None):
     """Masked GQA attention.  q [B,K,G,T,H], k/v [B,K,S,H] -> (o, lse).
 
     ``o`` is [B,K,G,T,H] float64 and ``lse`` [B,K,G,T] float64.  ``heads``
@@ -125,9 +140,12 @@ def attention_forward(q, k, v, *, causal: bool = False, seg_q=None,
             t_idx = np.arange(t0, t1)
             M = attention_mask(t_idx, s_all[:ns], causal,
                                None if sq is None else sq[b],
-                               None if skv is None else skv[b], off)
+                               None if skv is None else skv[b], off)[None]
+            hm = _head_mask(mask, kh, G, t_idx, s_all[:ns])
+            if hm is not None:
+                M = M & hm
             L = q[b, kh, :, t0:t1, :] @ k[b, kh, :ns, :].T       # [G, rb, ns]
-            W, l = masked_softmax(L, M[None])
+            W, l = masked_softmax(L, M)
             o[b, kh, :, t0:t1, :] = W @ v[b, kh, :ns, :]
             lse[b, kh, :, t0:t1] = l
     return o, lse
@@ -135,7 +153,7 @@ def attention_forward(q, k, v, *, causal: bool = False, seg_q=None,
 
 def attention_backward(q, k, v, dO, *, causal: bool = False, seg_q=None,
                        seg_kv=None, row_block: int = 512,
-                       heads: Optional[Sequence[tuple]] = None):
+                       heads: Optional[Sequence[tuple]] = None, mask=None):
     """Gradients of sum(O * dO) with respect to q, k, v (float64)."""
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     sq, skv = _i32(seg_q), _i32(seg_kv)
@@ -155,11 +173,14 @@ def attention_backward(q, k, v, dO, *, causal: bool = False, seg_q=None,
             t_idx = np.arange(t0, t1)
             M = attention_mask(t_idx, s_all[:ns], causal,
                                None if sq is None else sq[b],
-                               None if skv is None else skv[b], off)
+                               None if skv is None else skv[b], off)[None]
+            hm = _head_mask(mask, kh, G, t_idx, s_all[:ns])
+            if hm is not None:
+                M = M & hm
             qb = q[b, kh, :, t0:t1, :]                            # [G, rb, H]
             dOb = dO[b, kh, :, t0:t1, :]
             L = qb @ k[b, kh, :ns, :].T                           # [G, rb, ns]
-            W, _ = masked_softmax(L, M[None])
+            W, _ = masked_softmax(L, M)
             dP = dOb @ v[b, kh, :ns, :].T                         # [G, rb, ns]
             dS = W * (dP - (W * dP).sum(axis=-1, keepdims=True))
             dq[b, kh, :, t0:t1, :] = dS @ k[b, kh, :ns, :]
@@ -234,7 +255,7 @@ def attention_backward_rows(q, k, v, dO, b: int, kh: int, *, t_rows, s_rows,
 
 
 def attention_bruteforce(q, k, v, dO=None, *, causal: bool = False,
-                         seg_q=None, seg_kv=None):
+                         seg_q=None, seg_kv=None, mask=None):
     """Pure-Python loops over every (b, kv_head, g, t, s, h); tiny shapes only.
 
     Returns (o, lse) and, when ``dO`` is given, also (dq, dk, dv)."""
@@ -257,6 +278,9 @@ def attention_bruteforce(q, k, v, dO=None, *, causal: bool = False,
                         ok = (not causal) or s <= t + (S - T)
                         if sq is not None:
                             ok = ok and sq[b, t] == skv[b, s]
+                        if mask is not None:
+                            mh = 0 if len(mask) == 1 else kh * G + g
+                            ok = ok and bool(mask[mh][t][s])
                         if ok:
                             keep.append(s)
                     if not keep:

@@ -413,3 +413,35 @@ def test_unmasked_pair_count():
     for T, S in ((3, 9), (9, 3)):
         m = oa.attention_mask(np.arange(T), np.arange(S), True, None, None, S - T)
         assert inputs.unmasked_pairs(T, S, True, None, None) == int(m.sum())
+
+
+# ------------------------------------------------------ explicit masks
+
+def test_explicit_mask_matches_bruteforce_per_head():
+    B, K, G, T, S, H = 1, 2, 2, 6, 7, 3
+    q, k, v, dO = small(B, K, G, T, S, H, seed=81)
+    rng = np.random.default_rng(3)
+    mask = rng.random((K * G, T, S)) < 0.6
+    for causal in (False, True):
+        o, lse = oracle.attention_forward(q, k, v, causal=causal, mask=mask, row_block=4)
+        g = oracle.attention_backward(q, k, v, dO, causal=causal, mask=mask, row_block=4)
+        ref = oracle.attention_bruteforce(q, k, v, dO, causal=causal, mask=mask)
+        for a, r in zip((o, *g), (ref[0], ref[2], ref[3], ref[4])):
+            assert np.max(np.abs(a - r)) <= 1e-12
+        assert np.array_equal(np.isneginf(lse), np.isneginf(ref[1]))
+
+
+def test_explicit_mask_equal_to_causal_gives_causal():
+    q, k, v, dO = small(B=1, K=2, G=2, T=9, S=9, H=4, seed=82)
+    tri = np.tril(np.ones((9, 9), dtype=bool))[None]
+    a = oracle.attention_forward(q, k, v, mask=tri)
+    b = oracle.attention_forward(q, k, v, causal=True)
+    assert np.max(np.abs(a[0] - b[0])) <= 1e-14
+    ga = oracle.attention_backward(q, k, v, dO, mask=tri)
+    gb = oracle.attention_backward(q, k, v, dO, causal=True)
+    for x, y in zip(ga, gb):
+        assert np.max(np.abs(x - y)) <= 1e-13
+    full = np.ones((1, 9, 9), dtype=bool)
+    c = oracle.attention_forward(q, k, v, mask=full)
+    d = oracle.attention_forward(q, k, v)
+    assert np.max(np.abs(c[0] - d[0])) <= 1e-15
