@@ -38,6 +38,12 @@ SIGNATURES = {
                           ctypes.c_size_t, _I, _I, _I, _I, _I, _I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                             _I, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_masked": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
+                           _I, _I, _I, _I, _I, _I, _P]),
+    "fa_bwd_masked": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P,
+                           ctypes.c_size_t, _I, _I, _I, _I, _I, _I, _P]),
+    "fa_block_mask_build": (_I, [_P, _I, _I, _I, _P, _P, _P, ctypes.c_int64,
+                                 ctypes.POINTER(ctypes.c_int64)]),
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
@@ -189,7 +195,64 @@ def fa_device_sm_count() -> int:
     return int(load().fa_device_sm_count())
 
 
+def fa_block_mask_build(dense, heads, T, S, block_class, partial_index, partial_bits,
+                        partial_capacity) -> tuple:
+    """Host arrays in, (status, n_partial) out."""
+    n = ctypes.c_int64(0)
+    ptr = lambda a: None if a is None else ctypes.c_void_p(a.ctypes.data)
+    rc = load().fa_block_mask_build(ptr(dense), heads, T, S, ptr(block_class), ptr(partial_index),
+                                    ptr(partial_bits), int(partial_capacity), ctypes.byref(n))
+    return rc, int(n.value)
+
+
+def fa_fwd_masked(q, k, v, seg_q, seg_kv, causal, mask, o, lse, stream=None, check=True) -> int:
+    """`mask` = (block_class, partial_index, partial_bits, mask_heads), device tensors."""
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    cls, idx, bits, heads = mask
+    rc = load().fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(seg_q), _ptr(seg_kv),
+                              int(bool(causal)), _ptr(cls), _ptr(idx), _ptr(bits), int(heads),
+                              _ptr(o), _ptr(lse), B, K, G, T, S, H, _stream(stream))
+    if check:
+        _check("fa_fwd_masked", rc)
+    return rc
+
+
+def fa_bwd_masked(q, k, v, o, lse, dO, seg_q, seg_kv, causal, mask, dq, dk, dv, workspace,
+                  stream=None, check=True) -> int:
+    B, K, G, T, H = q.shape
+    S = k.shape[2]
+    cls, idx, bits, heads = mask
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().fa_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                              _ptr(seg_q), _ptr(seg_kv), int(bool(causal)), _ptr(cls), _ptr(idx),
+                              _ptr(bits), int(heads), _ptr(dq), _ptr(dk), _ptr(dv),
+                              _ptr(workspace), ws_bytes, B, K, G, T, S, H, _stream(stream))
+    if check:
+        _check("fa_bwd_masked", rc)
+    return rc
+
+
 # ------------------------------------------------------- tensor helpers
+
+def block_mask_from_dense(mask, device=None):
+    """Dense boolean mask [heads, T, S] -> (block_class, partial_index,
+    partial_bits, heads) built by fa_block_mask_build, as tensors on `device`."""
+    import numpy as np
+    dense = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+    heads, T, S = dense.shape
+    nqb, nkb = (T + 127) // 128, (S + 127) // 128
+    cls = np.zeros((heads, nqb, nkb), dtype=np.uint8)
+    idx = np.zeros((heads, nqb, nkb), dtype=np.int32)
+    rc, n = fa_block_mask_build(dense, heads, T, S, cls, idx, None, 0)
+    _check("fa_block_mask_build", rc)
+    bits = np.zeros((max(n, 1), 128, 4), dtype=np.uint32)
+    rc, n2 = fa_block_mask_build(dense, heads, T, S, cls, idx, bits, n)
+    _check("fa_block_mask_build", rc)
+    out = [torch.from_numpy(cls), torch.from_numpy(idx), torch.from_numpy(bits.view(np.int32))]
+    if device is not None:
+        out = [t.to(device) for t in out]
+    return out[0], out[1], out[2], heads
 
 def attention_forward(q, k, v, *, causal=False, seg_q=None, seg_kv=None, stream=None):
     """Allocate o / lse with torch and run fa_fwd.  Returns (o, lse)."""

@@ -112,11 +112,39 @@ int check_shapes(int B, int K, int G, int T, int S, int H, int causal, const voi
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
-           const int32_t* seg_kv, int causal, void* o, float* lse, int B, int K, int G, int T,
-           int S, int H, void* stream) {
+size_t splitkv_parts(int B, int K, int G, int T, int H, int n_splits, size_t* o_bytes) {
+  const size_t rows = (size_t)B * K * G * T;
+  const size_t ob = ((size_t)n_splits * rows * H * sizeof(float) + 255) & ~(size_t)255;
+  const size_t lb = ((size_t)n_splits * rows * sizeof(float) + 255) & ~(size_t)255;
+  if (o_bytes) *o_bytes = ob;
+  return ob + lb;
+}
+
+// Checks a block-mask argument set and fills `bm` (cls == nullptr: no mask).
+int make_block_mask(fa::BlockMask* bm, const uint8_t* cls, const int32_t* idx, const uint32_t* bits,
+                    int heads, int K, int G, int T, int S) {
+  *bm = fa::BlockMask{};
+  if (cls == nullptr && idx == nullptr && bits == nullptr) return FA_OK;
+  if (!cls || !idx || !bits) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(bits) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (heads != 1 && heads != K * G) return FA_ERR_INVALID_ARG;
+  bm->cls = cls;
+  bm->idx = idx;
+  bm->bits = bits;
+  bm->heads = heads;
+  bm->nqb = (T + 127) / 128;
+  bm->nkb = (S + 127) / 128;
+  return FA_OK;
+}
+
+// Shared body of the forward entry points.
+int fwd_common(const void* q, const void* k, const void* v, const int32_t* seg_q,
+               const int32_t* seg_kv, int causal, void* o, float* lse, const fa::BlockMask& bm,
+               int n_splits, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
+               int S, int H, void* stream) {
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
   // Pointers are required (and must be aligned) only for tensors with elements.
@@ -131,6 +159,12 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
   if (S == 0) {
     return fa::launch_fill_empty(o, lse, rows, H, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
+  size_t o_bytes = 0;
+  if (n_splits > 1) {
+    const size_t need = splitkv_parts(B, K, G, T, H, n_splits, &o_bytes);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return FA_ERR_INVALID_ARG;
+  }
   fa::FwdArgs a{};
   const int BK = B * K;
   if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
@@ -143,22 +177,42 @@ int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
   a.causal = causal ? 1 : 0;
   a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
-  a.n_splits = 1;
+  a.bm = bm;
+  a.n_splits = n_splits;
+  if (n_splits > 1) {
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  }
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
-  return fa::launch_fwd(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  cudaError_t e = fa::launch_fwd(a, st);
+  if (e == cudaSuccess && n_splits > 1)
+    e = fa::launch_split_combine(a.part_o, a.part_lse, n_splits, o, lse, rows, H, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-namespace {
-size_t splitkv_parts(int B, int K, int G, int T, int H, int n_splits, size_t* o_bytes) {
-  const size_t rows = (size_t)B * K * G * T;
-  const size_t ob = ((size_t)n_splits * rows * H * sizeof(float) + 255) & ~(size_t)255;
-  const size_t lb = ((size_t)n_splits * rows * sizeof(float) + 255) & ~(size_t)255;
-  if (o_bytes) *o_bytes = ob;
-  return ob + lb;
-}
 }  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, const int32_t* seg_q,
+           const int32_t* seg_kv, int causal, void* o, float* lse, int B, int K, int G, int T,
+           int S, int H, void* stream) {
+  return fwd_common(q, k, v, seg_q, seg_kv, causal, o, lse, fa::BlockMask{}, 1, nullptr, 0, B, K,
+                    G, T, S, H, stream);
+}
+
+int fa_fwd_masked(const void* q, const void* k, const void* v, const int32_t* seg_q,
+                  const int32_t* seg_kv, int causal, const uint8_t* block_class,
+                  const int32_t* partial_index, const uint32_t* partial_bits, int mask_heads,
+                  void* o, float* lse, int B, int K, int G, int T, int S, int H, void* stream) {
+  fa::BlockMask bm;
+  const int rc = make_block_mask(&bm, block_class, partial_index, partial_bits, mask_heads, K, G, T, S);
+  if (rc != FA_OK) return rc;
+  return fwd_common(q, k, v, seg_q, seg_kv, causal, o, lse, bm, 1, nullptr, 0, B, K, G, T, S, H,
+                    stream);
+}
 
 size_t fa_fwd_splitkv_workspace_size(int B, int K, int G, int T, int S, int H, int n_splits) {
   if (B <= 0 || K <= 0 || G <= 0 || T <= 0 || S < 0 || n_splits < 1 || n_splits > 256) return 0;
@@ -185,43 +239,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int32_t* s
                    void* workspace, size_t workspace_bytes, int B, int K, int G, int T, int S, int H,
                    void* stream) {
   if (n_splits < 1 || n_splits > 256) return FA_ERR_INVALID_ARG;
-  if (n_splits == 1)
-    return fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, B, K, G, T, S, H, stream);
-  const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
-  if (rc != FA_OK) return rc;
-  const long rows = (long)B * K * G * T;
-  const bool has_kv = (long)B * K * S > 0;
-  if (rows > 0 && (!q || !o || !lse || !aligned16(q) || !aligned16(o) ||
-                   (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
-    return FA_ERR_INVALID_ARG;
-  if (has_kv && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
-  if (rows == 0 || S == 0) return fa_fwd(q, k, v, seg_q, seg_kv, causal, o, lse, B, K, G, T, S, H, stream);
-  size_t o_bytes = 0;
-  const size_t need = splitkv_parts(B, K, G, T, H, n_splits, &o_bytes);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return FA_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  fa::FwdArgs a{};
-  const int BK = B * K;
-  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
-      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows) || !make_q_map(&a.tm_o, o, BK, G, T, H))
-    return FA_ERR_CUDA;
-  a.o = o;
-  a.lse = lse;
-  a.seg_q = seg_q;
-  a.seg_kv = seg_kv;
-  a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
-  a.causal = causal ? 1 : 0;
-  a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
-  a.n_splits = n_splits;
-  a.part_o = static_cast<float*>(workspace);
-  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
-  a.err = error_word();
-  a.wait_limit_ns = wait_limit();
-  if (!a.err) return FA_ERR_CUDA;
-  cudaError_t e = fa::launch_fwd(a, st);
-  if (e == cudaSuccess) e = fa::launch_split_combine(a.part_o, a.part_lse, n_splits, o, lse, rows, H, st);
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return fwd_common(q, k, v, seg_q, seg_kv, causal, o, lse, fa::BlockMask{}, n_splits, workspace,
+                    workspace_bytes, B, K, G, T, S, H, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {
@@ -234,9 +253,9 @@ namespace {
 
 // Shared body of fa_bwd and fa_bwd_stage: stage < 0 runs every stage.
 int bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o, const float* lse,
-             const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
-             void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
-             int S, int H, void* stream) {
+             const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal,
+             const fa::BlockMask& bm, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int K, int G, int T, int S, int H, void* stream) {
   if (stage < -1 || stage > 2) return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
@@ -284,6 +303,7 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.causal = causal ? 1 : 0;
   a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
   a.n_kvtiles = (S + kvr - 1) / kvr;
+  a.bm = bm;
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
@@ -304,8 +324,68 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal, void* dq,
            void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
            int S, int H, void* stream) {
-  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
+  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
+                  workspace, workspace_bytes, B, K, G, T, S, H, stream);
+}
+
+int fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                  const uint8_t* block_class, const int32_t* partial_index,
+                  const uint32_t* partial_bits, int mask_heads, void* dq, void* dk, void* dv,
+                  void* workspace, size_t workspace_bytes, int B, int K, int G, int T, int S, int H,
+                  void* stream) {
+  fa::BlockMask bm;
+  const int rc = make_block_mask(&bm, block_class, partial_index, partial_bits, mask_heads, K, G, T, S);
+  if (rc != FA_OK) return rc;
+  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, bm, dq, dk, dv, workspace,
                   workspace_bytes, B, K, G, T, S, H, stream);
+}
+
+int fa_block_mask_build(const uint8_t* dense, int heads, int T, int S, uint8_t* block_class,
+                        int32_t* partial_index, uint32_t* partial_bits, int64_t partial_capacity,
+                        int64_t* n_partial) {
+  if (!dense || !block_class || !partial_index || !n_partial || heads < 1 || T < 1 || S < 1 ||
+      partial_capacity < 0 || (partial_capacity > 0 && !partial_bits))
+    return FA_ERR_INVALID_ARG;
+  const int nqb = (T + 127) / 128, nkb = (S + 127) / 128;
+  int64_t count = 0;
+  for (int h = 0; h < heads; ++h) {
+    for (int qb = 0; qb < nqb; ++qb) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int t0 = qb * 128, t1 = t0 + 128 < T ? t0 + 128 : T;
+        const int s0 = kb * 128, s1 = s0 + 128 < S ? s0 + 128 : S;
+        long kept = 0;
+        for (int t = t0; t < t1; ++t) {
+          const uint8_t* row = dense + ((long)h * T + t) * S;
+          for (int s = s0; s < s1; ++s) kept += row[s] != 0;
+        }
+        const long total = (long)(t1 - t0) * (s1 - s0);
+        const long blk = ((long)h * nqb + qb) * nkb + kb;
+        partial_index[blk] = -1;
+        if (kept == 0) {
+          block_class[blk] = 0;  // EMPTY: the kernels skip the tile
+        } else if (kept == total) {
+          block_class[blk] = 1;  // FULL: no per-element mask
+        } else {
+          block_class[blk] = 2;  // PARTIAL: 128 x 128 bits, row-major, 4 words per row
+          if (count < partial_capacity) {
+            uint32_t* bits = partial_bits + count * 128 * 4;
+            for (int i = 0; i < 128 * 4; ++i) bits[i] = 0;
+            for (int t = t0; t < t1; ++t) {
+              const uint8_t* row = dense + ((long)h * T + t) * S;
+              for (int s = s0; s < s1; ++s)
+                if (row[s]) bits[(t - t0) * 4 + (s - s0) / 32] |= 1u << ((s - s0) % 32);
+            }
+          }
+          partial_index[blk] = (int32_t)count;
+          ++count;
+        }
+      }
+    }
+  }
+  *n_partial = count;
+  if (partial_bits != nullptr && count > partial_capacity) return FA_ERR_INVALID_ARG;
+  return FA_OK;
 }
 
 int fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
@@ -313,8 +393,8 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const v
                  int causal, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                  int B, int K, int G, int T, int S, int H, void* stream) {
   if (stage < 0) return FA_ERR_INVALID_ARG;
-  return bwd_impl(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, workspace,
-                  workspace_bytes, B, K, G, T, S, H, stream);
+  return bwd_impl(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
+                  workspace, workspace_bytes, B, K, G, T, S, H, stream);
 }
 
 // ------------------------------------------------------------------------
@@ -352,8 +432,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
     return FA_ERR_UNSUPPORTED;
   void* scratch = noalloc_scratch_address();
   if (scratch == nullptr) return FA_ERR_CUDA;
-  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, dq, dk, dv, scratch,
-                  (size_t)FA_NOALLOC_SCRATCH_BYTES, B, K, G, T, S, H, stream);
+  return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
+                  scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES, B, K, G, T, S, H, stream);
 }
 
 int fa_check_status(void* stream) {

@@ -18,6 +18,7 @@
 // and in exchange need no atomics: every output element is written once by
 // one CTA, so the result is deterministic.
 #include <cuda_bf16.h>
+#include "block_mask.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -40,7 +41,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const A
 // (conservative for non-monotone ids).  Keys past S on a ragged last tile
 // make it PARTIAL; query rows past T are handled by their -inf lse instead.
 __device__ __forceinline__ int tile_class(const BwdArgs& a, const int2* qr, const int2* kr, int b,
-                                          int qt, int jt, int Tb, int kvr) {
+                                          int kh, int qt, int jt, int Tb, int kvr) {
   const int t0 = qt * Tb, s0 = jt * kvr;
   const int t_last = min(t0 + Tb, a.T) - 1, s_last = min(s0 + kvr, a.S) - 1;
   const int off = a.S - a.T;
@@ -56,6 +57,8 @@ __device__ __forceinline__ int tile_class(const BwdArgs& a, const int2* qr, cons
     if (k.y < q.x || k.x > q.y) return TILE_EMPTY;
     if (!(q.x == q.y && k.x == k.y && q.x == k.x)) c = TILE_PARTIAL;
   }
+  if (a.bm.cls != nullptr)  // the Q tile lies in one mask block; kv tiles of <= 128 keys too
+    c = class_and(c, bm_tile_class(a.bm, kh, a.G, t0 >> 7, s0 >> 7));
   return c;
 }
 
@@ -76,8 +79,8 @@ __device__ __forceinline__ int causal_kv_end(const BwdArgs& a, int t0, int Tb, i
 
 // Apply the causal / segment / key-range mask to 32 consecutive key columns
 // [scol, scol + 32) of the row at position t.
-__device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int t, int my_seg,
-                                       int scol) {
+__device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int kh, int g, int t,
+                                       int my_seg, int scol) {
   const int off = a.S - a.T;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -101,6 +104,12 @@ __device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, 
       for (int i = 0; i < 32; ++i)
         if (scol + i < a.S && __ldg(ids + i) != my_seg) s[i] = -INFINITY;
     }
+  }
+  if (a.bm.cls != nullptr && t < a.T) {
+    const uint32_t bits = bm_row_word(a.bm, kh, a.G, g, t, scol >> 7, (scol & 127) >> 5);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!((bits >> i) & 1u)) s[i] = -INFINITY;
   }
 }
 
@@ -188,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       uint32_t k_issued = 0, v_issued = 0;
       bool any = false;
       for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!any) {
           any = true;
           mbar_arrive_expect_tx(q_full(), 2 * HC * kQChunk);
@@ -250,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         return true;
       };
       for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!waited_q) {
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
       bool ok = true, waited_q = false;
       int n = 0;
       for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!waited_q) {
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
@@ -334,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
     bool ok = true;
     int n = 0;
     for (int jt = 0; jt < jt_end; ++jt) {
-      const int cls = tile_class(a, qr, kr, b, qt, jt, Tb, BN);
+      const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int u = n % NBUF;
       if (!warp_wait(sdp_full(u), (n / NBUF) & 1, ab)) { ok = false; break; }
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         tmem_ld32(tmem + lane_base + C::dp_col(u) + c * 32, pv);
         tmem_wait_ld();
         float* s = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, t, my_seg, jt * BN + c * 32);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, jt * BN + c * 32);
         uint32_t ds[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -478,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       int i = 0;
       uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
-        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!any) {
           any = true;
           mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       bool ok = true;
       int i = 0;
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
-        if (tile_class(a, qr, kr, b, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
         // This issuer's S (or dP) columns of the previous tile were read before
         // the softmax side signalled ps_full, which it waited for below.
@@ -572,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     bool ok = true;
     int i = 0;
     for (int qt = qt_begin; qt < a.n_qtiles; ++qt) {
-      const int cls = tile_class(a, qr, kr, b, qt, jt, Tb, BN);
+      const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int g = r / Tb, t = qt * Tb + (r - g * Tb);
       const bool valid = t < a.T;  // rows past T (ragged last tile) are inert
@@ -597,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
         tmem_wait_ld();
         float* s = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, t, my_seg, s0 + c * 32);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {

@@ -21,6 +21,7 @@
 // kSlots chunks of [128 keys x 64 dims] bf16 fed by TMA with 128-byte swizzle,
 // the per-tile schedule and the mbarriers.
 #include <cuda_bf16.h>
+#include "block_mask.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -178,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       if (mx < qmn || mn > qmx) c = TILE_EMPTY;
       else if (!(mn == mx && qmn == qmx && mn == qmn)) c = TILE_PARTIAL;
     }
+    if (a.bm.cls != nullptr)  // the Q tile lies inside one 128-position mask block
+      c = (uint8_t)class_and(c, bm_tile_class(a.bm, bk % a.K, a.G, t0 >> 7, j));
     if (lane == 0) cls[j] = c;
   }
   __syncthreads();
@@ -344,6 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (s0 + c < a.S && __ldg(ids + c) != my_seg) s[c] = -INFINITY;
+          }
+        }
+        if (a.bm.cls != nullptr && valid) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t bits = bm_row_word(a.bm, bk % a.K, a.G, g, t, j, w);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!((bits >> i) & 1u)) s[32 * w + i] = -INFINITY;
           }
         }
       }

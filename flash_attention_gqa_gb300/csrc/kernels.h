@@ -11,6 +11,15 @@ constexpr int kRows = 128;     // packed query rows per Q tile (G heads x 128/G 
 constexpr int kKvRows = 128;   // key/value rows per KV tile in the forward
 constexpr int kMaxKvTiles = 1024;  // S <= 131072
 
+// Block-sparse mask metadata (device pointers; cls == nullptr: no mask).
+struct BlockMask {
+  const uint8_t* cls;     // [heads, nqb, nkb] EMPTY / FULL / PARTIAL
+  const int32_t* idx;     // [heads, nqb, nkb] bitmask index of PARTIAL blocks
+  const uint32_t* bits;   // [n_partial, 128, 4]
+  int heads;              // 1 or K*G
+  int nqb, nkb;           // ceil(T / 128), ceil(S / 128)
+};
+
 struct FwdArgs {
   CUtensorMap tm_q;   // q as 4-D {H, T, G, B*K}, box {64, 128/G, G, 1}, 128B swizzle
   CUtensorMap tm_k;   // k as 3-D {H, S, B*K},   box {64, 128, 1}
@@ -23,6 +32,7 @@ struct FwdArgs {
   int B, K, G, T, S, H;
   int causal;
   int n_qtiles;       // ceil(T / (128 / G))
+  BlockMask bm;
   int n_splits;       // > 1: split-KV mode (grid.z splits the KV-tile schedule)
   float* part_o;      // split-KV: fp32 [n_splits, B*K*G*T, H] partial outputs
   float* part_lse;    // split-KV: [n_splits, B*K*G*T] partial lse (natural log)
@@ -47,6 +57,7 @@ struct BwdArgs {
   int causal;
   int n_qtiles;        // T / (128 / G)
   int n_kvtiles;       // S / kv_rows
+  BlockMask bm;
   uint32_t* err;
   uint64_t wait_limit_ns;
 };

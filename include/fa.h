@@ -92,6 +92,50 @@ size_t fa_fwd_splitkv_workspace_size(int B, int K, int G, int T, int S, int H, i
    at most the number of KV tiles. */
 int fa_fwd_splitkv_default_splits(int B, int K, int G, int T, int S, int H);
 
+/*
+ * Block-sparse masks (lazy, per block): a mask over query heads is described
+ * by blocks of 128 query positions x 128 keys instead of a T x S array, in the
+ * spirit of splash attention's per-block mask info (MultiHeadMask /
+ * process_mask, "Our first kernel" baseline).  For each mask head h (one head
+ * shared by every query head, mask_heads == 1, or one per query head,
+ * mask_heads == K*G with h = k*G + g) and block (qb, kb):
+ *   block_class[h][qb][kb]   uint8: 0 EMPTY (skipped), 1 FULL, 2 PARTIAL
+ *   partial_index[h][qb][kb] int32: index of the block's bitmask (PARTIAL)
+ *   partial_bits[i][r][w]    uint32: bit j of word w = key 32*w + j of query
+ *                            row r of bitmask i (128 rows x 4 words)
+ * with nqb = ceil(T/128), nkb = ceil(S/128).  The mask is ANDed with the
+ * causal and segment masks; all three arrays live in device memory.
+ * fa_block_mask_build() fills them (host memory) from a dense host mask.
+ */
+int fa_fwd_masked(const void* q, const void* k, const void* v,
+                  const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                  const uint8_t* block_class, const int32_t* partial_index,
+                  const uint32_t* partial_bits, int mask_heads,
+                  void* o, float* lse,
+                  int B, int K, int G, int T, int S, int H, void* stream);
+
+int fa_bwd_masked(const void* q, const void* k, const void* v,
+                  const void* o, const float* lse, const void* dO,
+                  const int32_t* seg_q, const int32_t* seg_kv, int causal,
+                  const uint8_t* block_class, const int32_t* partial_index,
+                  const uint32_t* partial_bits, int mask_heads,
+                  void* dq, void* dk, void* dv,
+                  void* workspace, size_t workspace_bytes,
+                  int B, int K, int G, int T, int S, int H, void* stream);
+
+/*
+ * Host-side builder of the block metadata from a dense host mask
+ * dense[heads][T][S] (nonzero = keep).  Writes block_class and partial_index
+ * ([heads][nqb][nkb]) and up to partial_capacity bitmasks into partial_bits;
+ * *n_partial receives the number of PARTIAL blocks.  Call it first with
+ * partial_bits = NULL and partial_capacity = 0 to size partial_bits.
+ * Returns FA_ERR_INVALID_ARG on bad arguments or too small a capacity.
+ */
+int fa_block_mask_build(const uint8_t* dense, int heads, int T, int S,
+                        uint8_t* block_class, int32_t* partial_index,
+                        uint32_t* partial_bits, int64_t partial_capacity,
+                        int64_t* n_partial);
+
 /* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256;
    0 for empty or unsupported sizes). */
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
