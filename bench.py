@@ -63,8 +63,11 @@ def parse_args():
 
 # ------------------------------------------------------------- bookkeeping
 
-def flop_counts(w: inputs.Workload, seg: np.ndarray | None):
-    pairs = inputs.unmasked_pairs(w.T, w.S, w.causal, seg, seg, B=w.B)
+def flop_counts(w: inputs.Workload, seg: np.ndarray | None, dense_mask=None):
+    if dense_mask is not None:   # the mask already encodes causality and the window
+        pairs = int(dense_mask.sum()) * w.B
+    else:
+        pairs = inputs.unmasked_pairs(w.T, w.S, w.causal, seg, seg, B=w.B)
     fwd = 4.0 * w.K * w.G * w.H * pairs
     return fwd, (2.5 * fwd if w.backward else 0.0), pairs / (w.B * w.T * w.S)
 
@@ -139,7 +142,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle
 
-def oracle_sample(w: inputs.Workload, x: inputs.Tensors, rows: int):
+def oracle_sample(w: inputs.Workload, x: inputs.Tensors, rows: int, dense_mask=None):
     """The first `rows` query positions of the workload (with the keys they can
     see when causal) as a self-contained sub-problem for the CPU oracle."""
     rows = min(rows, w.T)
@@ -151,7 +154,15 @@ def oracle_sample(w: inputs.Workload, x: inputs.Tensors, rows: int):
                seg_kv=None if x.seg_kv is None else sl(x.seg_kv, 1, nkeys))
     segq = None if sub["seg_q"] is None else sub["seg_q"].numpy()
     segk = None if sub["seg_kv"] is None else sub["seg_kv"].numpy()
-    pairs = inputs.unmasked_pairs(rows, nkeys, w.causal, segq, segk, B=w.B)
+    if w.kind == "decode":
+        nkeys = w.S   # one query against the whole cache
+        sub.update(k=x.k, v=x.v)
+    sub["mask"] = None
+    if dense_mask is not None:
+        sub["mask"] = dense_mask[:, :rows, :nkeys]
+        pairs = int(sub["mask"].sum()) * w.B
+    else:
+        pairs = inputs.unmasked_pairs(rows, nkeys, w.causal, segq, segk, B=w.B)
     fwd = 4.0 * w.K * w.G * w.H * pairs
     flop = fwd * (3.5 if w.backward else 1.0)
     desc = (f"first {rows} of {w.T} query positions x all {w.B * w.K * w.G} heads "
@@ -162,14 +173,14 @@ def oracle_sample(w: inputs.Workload, x: inputs.Tensors, rows: int):
 
 def run_oracle_step(w, sub):
     import oracle  # the CPU oracle: only the baseline / reference legs use it
-    kw = dict(causal=w.causal, seg_q=sub["seg_q"], seg_kv=sub["seg_kv"])
+    kw = dict(causal=w.causal, seg_q=sub["seg_q"], seg_kv=sub["seg_kv"], mask=sub["mask"])
     oracle.attention_forward(sub["q"], sub["k"], sub["v"], **kw)
     if w.backward:
         oracle.attention_backward(sub["q"], sub["k"], sub["v"], sub["dO"], **kw)
 
 
-def cpu_baseline(w, x, rows):
-    sub, flop, desc = oracle_sample(w, x, rows)
+def cpu_baseline(w, x, rows, dense_mask=None):
+    sub, flop, desc = oracle_sample(w, x, rows, dense_mask)
     t = time.perf_counter()
     run_oracle_step(w, sub)
     dt = time.perf_counter() - t
@@ -206,18 +217,19 @@ def reference_arm(args, world, rank):
         return
     w = inputs.WORKLOADS[args.workload]
     x = inputs.make_workload(w)
+    dense_mask = inputs.window_mask(w.T, w.S, w.window) if w.kind == "window" else None
     # Size the sample so the whole run stays within about two and a half
     # minutes: time a 256-row sample once (untimed) and scale by the causal
     # (quadratic) or linear growth of the work with the number of rows.
     budget = 150.0 / max(1, args.steps + args.warmup)
-    probe, _, _ = oracle_sample(w, x, 256)
+    probe, _, _ = oracle_sample(w, x, 256, dense_mask)
     t = time.perf_counter()
     run_oracle_step(w, probe)
     t256 = max(time.perf_counter() - t, 1e-3)
     growth = 0.5 if w.causal else 1.0
     rows = int(256 * (budget / t256) ** growth) // 128 * 128
-    rows = max(128, min(rows, 2048, w.T))
-    sub, flop, desc = oracle_sample(w, x, rows)
+    rows = max(1, min(max(rows, 128), 2048, w.T))
+    sub, flop, desc = oracle_sample(w, x, rows, dense_mask)
     for _ in range(args.warmup):
         run_oracle_step(w, sub)
     t = time.perf_counter()
@@ -250,8 +262,15 @@ def ours_arm(args, world, rank, local):
     w = inputs.WORKLOADS[args.workload]
     x = inputs.make_workload(w)
     seg_np = None if x.seg_q is None else x.seg_q.numpy()
-    fwd_flop, bwd_flop, frac = flop_counts(w, seg_np)
+    dense_mask = inputs.window_mask(w.T, w.S, w.window) if w.kind == "window" else None
+    fwd_flop, bwd_flop, frac = flop_counts(w, seg_np, dense_mask)
     step_flop = fwd_flop + bwd_flop
+    meta = None
+    if dense_mask is not None:
+        meta = binding.block_mask_from_dense(dense_mask, device=dev)
+    n_splits = 1
+    if w.kind == "decode":
+        n_splits = binding.fa_fwd_splitkv_default_splits(w.B, w.K, w.G, w.T, w.S, w.H)
 
     q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
     dO = x.dO.to(dev) if w.backward else None
@@ -264,17 +283,33 @@ def ours_arm(args, world, rank, local):
         ws = torch.empty(max(256, binding.fa_bwd_workspace_size(w.B, w.K, w.G, w.T, w.S, w.H)),
                          dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    n_kernels = 1 + ((1 + (2 if sq is not None else 0) + 2) if w.backward else 0)
-    names = ["fa_fwd_kernel", "bwd_preprocess", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"]
+    if n_splits > 1:
+        ws_split = torch.empty(binding.fa_fwd_splitkv_workspace_size(w.B, w.K, w.G, w.T, w.S, w.H,
+                                                                     n_splits),
+                               dtype=torch.uint8, device=dev)
+    n_kernels = 1 + (1 if n_splits > 1 else 0) + \
+        ((1 + (2 if sq is not None else 0) + 2) if w.backward else 0)
     n_ev = 5 if w.backward else 2
 
     def step(evs=None):
         if evs is not None:
             evs[0].record(stream)
-        binding.fa_fwd(q, k, v, sq, skv, w.causal, o, lse, stream)
+        if meta is not None:
+            binding.fa_fwd_masked(q, k, v, sq, skv, w.causal, meta, o, lse, stream)
+        elif n_splits > 1:
+            binding.fa_fwd_splitkv(q, k, v, sq, skv, w.causal, o, lse, n_splits, ws_split, stream)
+        else:
+            binding.fa_fwd(q, k, v, sq, skv, w.causal, o, lse, stream)
         if evs is not None:
             evs[1].record(stream)
-        if w.backward:
+        if w.backward and meta is not None:
+            # the masked backward runs its stages back to back (one call)
+            binding.fa_bwd_masked(q, k, v, o, lse, dO, sq, skv, w.causal, meta, dq, dk, dv, ws,
+                                  stream)
+            if evs is not None:
+                for i in (2, 3, 4):
+                    evs[i].record(stream)
+        elif w.backward:
             for st in range(3):
                 binding.fa_bwd_stage(st, q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws,
                                      stream)
@@ -316,19 +351,34 @@ def ours_arm(args, world, rank, local):
     # dP, dV, dK products (2x fwd); dQ = S, dP, dQ products (1.5x fwd)
     kflop = {"fa_fwd_kernel": fwd_flop, "fa_bwd_dkdv_kernel": 2.0 * fwd_flop,
              "fa_bwd_dq_kernel": 1.5 * fwd_flop}
+    if meta is not None and w.backward:   # one timed block for the whole masked backward
+        per = {"fa_fwd_kernel": per["fa_fwd_kernel"],
+               "fa_bwd_masked (all stages)": per["bwd_preprocess"] + per["fa_bwd_dkdv_kernel"]
+               + per["fa_bwd_dq_kernel"]}
+        kflop = {"fa_fwd_kernel": fwd_flop}
     top = max((n for n in per if n in kflop), key=lambda n: per[n])
     burst, sustained, hbm, src = measured_peaks()
     timed_s = ms * args.steps / 1e3
     peak = burst if timed_s < 1.0 else sustained
-    achieved = kflop[top] / (per[top] * 1e-3) / 1e12
     src_file = "fwd.cu" if top == "fa_fwd_kernel" else "bwd.cu"
     tr = NCU_TRAFFIC.get(top)
     traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(src_file) else None
-    roofline = {"bound": "tensor", "kernel": top, "achieved": round(achieved, 1),
-                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic,
-                "peak_source": f"{src} bf16 {'burst' if peak == burst else 'sustained'}",
-                "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
+    if w.kind == "decode":
+        # memory-bound: K and V are read once, q / o / lse move once
+        fbytes = 2 * (x.k.numel() + x.v.numel() + 2 * x.q.numel()) + 4 * lse.numel()
+        achieved = fbytes / (per["fa_fwd_kernel"] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "fa_fwd_kernel (split-KV x%d) + merge" % n_splits,
+                    "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(achieved / hbm, 4), "traffic": None,
+                    "algorithmic_bytes": fbytes, "peak_source": f"{src} HBM copy",
+                    "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
+    else:
+        achieved = kflop[top] / (per[top] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": top, "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": traffic,
+                    "peak_source": f"{src} bf16 {'burst' if peak == burst else 'sustained'}",
+                    "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
 
     # end to end through the C ABI with host buffers: H2D inputs, D2H outputs
     host_in = [t.pin_memory() for t in (x.q, x.k, x.v) + ((x.dO,) if w.backward else ())]
@@ -373,6 +423,8 @@ def ours_arm(args, world, rank, local):
                    "fwd_tflops": round(fwd_flop / (per["fa_fwd_kernel"] * 1e-3) / 1e12, 1),
                    "bwd_tflops": (round(bwd_flop / ((ms - per["fa_fwd_kernel"]) * 1e-3) / 1e12, 1)
                                   if w.backward else None),
+                   "kind": w.kind, "split_kv": n_splits if n_splits > 1 else None,
+                   "window": w.window or None,
                    "pct_of_peak": round(100 * step_flop / (ms * 1e-3) / 1e12 / peak, 2),
                    "l2": f"inputs+outputs {in_bytes / 2**20:.0f} MiB vs L2 {L2_BYTES / 2**20:.0f} MiB"
                          + (" (larger: no flush)" if in_bytes > L2_BYTES else " (smaller than L2)"),
@@ -385,7 +437,7 @@ def ours_arm(args, world, rank, local):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_rows)
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_rows, dense_mask)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -42,6 +42,8 @@ class Workload:
     backward: bool = True
     seed: int = 0
     doc_len: tuple = (128, 2048)
+    kind: str = "dense"      # "dense", "decode" (split-KV forward) or "window" (block-sparse)
+    window: int = 0          # "window": keys t - window < s <= t (with causal)
 
     @property
     def scale(self) -> float:
@@ -63,7 +65,23 @@ WORKLOADS = {
     "gqa_packed_docs_h128_t4096": Workload("gqa_packed_docs_h128_t4096", 4, 8,
                                            4, 4096, 4096, 128, causal=True,
                                            segments=True),
+    # One decode step (T = 1) against a 32k-key cache: memory-bound.
+    "gqa_decode_h128_s32768": Workload("gqa_decode_h128_s32768", 8, 8, 8, 1, 32768, 128,
+                                       causal=True, backward=False, kind="decode"),
+    # Causal sliding window of 1024 keys given as a block-sparse mask.
+    "gqa_window1024_h128_t8192": Workload("gqa_window1024_h128_t8192", 1, 8, 4, 8192, 8192,
+                                          128, causal=True, kind="window", window=1024),
 }
+
+
+def window_mask(T: int, S: int, window: int) -> np.ndarray:
+    """Dense [1, T, S] keep-mask of a causal sliding window: t - window < s <= t + (S - T).
+
+    A mask *layout* (which pairs exist), not attention arithmetic."""
+    off = S - T
+    t = np.arange(T)[:, None]
+    s = np.arange(S)[None, :]
+    return ((s <= t + off) & (s > t + off - window))[None]
 
 
 def document_segment_ids(batch: int, length: int, seed: int,
