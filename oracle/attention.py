@@ -209,33 +209,43 @@ def attention_backward_rows(q, k, v, dO, b: int, kh: int, *, t_rows, s_rows,
     """Sampled gradients of one (b, kv_head): dq at query rows ``t_rows`` (all
     G heads) and dk, dv at key rows ``s_rows``.
 
-    dk/dv at a key need every query's softmax normaliser and rowsum(W * dP),
-    so those two per-row statistics are computed for all rows first (blocked
-    over query rows, the same definition as ``attention_backward``)."""
+    dk/dv at a key need the softmax normaliser and rowsum(W * dP) of every
+    query that sees the key, so those two per-row statistics are computed
+    first (blocked over query rows, the same definition as
+    ``attention_backward``) for the rows that matter."""
     qh, kk, vv, dOh = _f64(q[b, kh]), _f64(k[b, kh]), _f64(v[b, kh]), _f64(dO[b, kh])
     sq, skv = _i32(seg_q), _i32(seg_kv)
     G, T, H = qh.shape
     S = kk.shape[0]
     sqb = None if sq is None else sq[b]
     skb = None if skv is None else skv[b]
-    lse = np.empty((G, T))
-    delta = np.empty((G, T))
-    s_all = np.arange(S)
+    t_rows = np.asarray(t_rows)
+    s_rows = np.asarray(s_rows)
     off = S - T
+    # Rows whose statistics are needed: the sampled query rows, and every row
+    # that can see a sampled key.  Under the causal mask a row t sees key s
+    # only if s <= t + off, so rows t < min(s_rows) - off contribute exactly
+    # zero to the sampled dk / dv and are skipped (lse stays -inf there).
+    need = np.zeros(T, dtype=bool)
+    need[t_rows] = True
+    if causal:
+        need[max(0, int(s_rows.min()) - off):] = True
+    else:
+        need[:] = True
+    lse = np.full((G, T), NEG_INF)
+    delta = np.zeros((G, T))
+    s_all = np.arange(S)
     for t0, t1 in _row_blocks(T, row_block):
+        if not need[t0:t1].any():
+            continue
         ns = _key_range(t1, S, causal, off)
         if ns == 0:
-            lse[:, t0:t1] = NEG_INF
-            delta[:, t0:t1] = 0.0
             continue
         M = attention_mask(np.arange(t0, t1), s_all[:ns], causal, sqb, skb, off)
         W, l = masked_softmax(qh[:, t0:t1] @ kk[:ns].T, M[None])
         dP = dOh[:, t0:t1] @ vv[:ns].T
         lse[:, t0:t1] = l
         delta[:, t0:t1] = (W * dP).sum(axis=-1)
-
-    t_rows = np.asarray(t_rows)
-    s_rows = np.asarray(s_rows)
     # dq rows: full key range for the sampled query rows
     M = attention_mask(t_rows, s_all, causal, sqb, skb, off)
     Wt, _ = masked_softmax(qh[:, t_rows] @ kk.T, M[None])

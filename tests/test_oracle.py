@@ -323,6 +323,21 @@ def test_sampled_rows_match_full():
     assert np.max(np.abs(l3 - lse[1, 1])) <= 1e-12
 
 
+def test_sampled_late_keys_skip_rows_exactly():
+    # with only late sampled keys, rows that cannot see them are skipped; the
+    # sampled dk / dv / dq must not change
+    B, K, G, T, H = 1, 1, 2, 96, 8
+    q, k, v, dO = small(B, K, G, T, T, H, seed=53)
+    dq, dk, dv = oracle.attention_backward(q, k, v, dO, causal=True)
+    rows, srows = [3, 50, 95], [70, 80, 95]
+    gq, gk, gv, lse, _ = oracle.attention_backward_rows(q, k, v, dO, 0, 0, t_rows=rows,
+                                                        s_rows=srows, row_block=16, causal=True)
+    assert np.max(np.abs(gq - dq[0, 0][:, rows])) <= 1e-12
+    assert np.max(np.abs(gk - dk[0, 0][srows])) <= 1e-12
+    assert np.max(np.abs(gv - dv[0, 0][srows])) <= 1e-12
+    assert np.isneginf(lse[:, 20]).all()        # a skipped row (no sampled key visible)
+
+
 def test_row_block_size_does_not_matter():
     q, k, v, dO = small(B=1, K=1, G=3, T=33, S=33, H=6, seed=61)
     a = oracle.attention_backward(q, k, v, dO, causal=True, row_block=1)
