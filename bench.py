@@ -309,19 +309,21 @@ def ours_arm(args, world, rank, local):
             if evs is not None:
                 for i in (2, 3, 4):
                     evs[i].record(stream)
+        elif w.backward and evs is None:
+            # one call: the dQ grid may overlap the tail of the dK/dV grid
+            binding.fa_bwd(q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws, stream)
         elif w.backward:
+            # stage by stage with events between them: per-kernel durations
             for st in range(3):
                 binding.fa_bwd_stage(st, q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws,
                                      stream)
-                if evs is not None:
-                    evs[2 + st].record(stream)
+                evs[2 + st].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert binding.fa_check_status(stream) == binding.FA_OK
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -330,7 +332,7 @@ def ours_arm(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        step(events[i])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -340,7 +342,13 @@ def ours_arm(args, world, rank, local):
     assert status == binding.FA_OK, binding.status_string(status)
     ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dev)
 
-    # per-kernel device time (mean over the timed steps)
+    # per-kernel device time: a second loop, stage by stage with CUDA events
+    # between the launches (which also keeps dQ from overlapping dK/dV there)
+    n_k = max(3, min(args.steps, 20))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_k)]
+    for i in range(n_k):
+        step(events[i])
+    torch.cuda.synchronize()
     per = {}
     per["fa_fwd_kernel"] = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
     if w.backward:

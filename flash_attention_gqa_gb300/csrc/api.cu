@@ -107,6 +107,7 @@ int check_shapes(int B, int K, int G, int T, int S, int H, int causal, const voi
   if (!pow2_le128(G)) return FA_ERR_UNSUPPORTED;
   if ((S + fa::kKvRows - 1) / fa::kKvRows > fa::kMaxKvTiles) return FA_ERR_UNSUPPORTED;
   if ((long long)B * K > 65535) return FA_ERR_UNSUPPORTED;
+  if ((long long)T * B * K > (1LL << 31) - 1) return FA_ERR_UNSUPPORTED;  // flat grids
   return FA_OK;
 }
 
@@ -313,7 +314,9 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
     if (e == cudaSuccess) e = fa::launch_seg_ranges(a, st);
   }
   if (e == cudaSuccess && (stage < 0 || stage == 1)) e = fa::launch_bwd_dkdv(a, st);
-  if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq(a, st);
+  // All stages in one call: the dQ grid directly follows the dK/dV grid and may
+  // overlap its tail (both read only stage 0's results and the inputs).
+  if (e == cudaSuccess && (stage < 0 || stage == 2)) e = fa::launch_bwd_dq(a, st, stage < 0);
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

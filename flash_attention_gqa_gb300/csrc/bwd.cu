@@ -162,8 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Tb = kRows / a.G;
-  const int qt = a.n_qtiles - 1 - (int)blockIdx.x;
-  const int bk = blockIdx.y, b = bk / a.K;
+  // Flat grid, Q-tile major: latest (causally heaviest) Q tiles of every head first.
+  const int BKn = a.B * a.K;
+  const int qt = a.n_qtiles - 1 - (int)(blockIdx.x / BKn);
+  const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
   const int t0 = qt * Tb;
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
@@ -455,8 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Tb = kRows / a.G;
-  const int jt = blockIdx.x;  // kv tile; early (causally heaviest) tiles first
-  const int bk = blockIdx.y, b = bk / a.K;
+  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head first.
+  const int BKn = a.B * a.K;
+  const int jt = (int)(blockIdx.x / BKn);
+  const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
+  // The dQ kernel reads nothing this kernel writes: let it be scheduled on SMs
+  // this grid frees in its tail (it is launched with programmatic serialization).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int s0 = jt * BN;
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
@@ -725,12 +732,21 @@ cudaError_t set_smem(Kern k, uint32_t bytes, int* configured) {
 }
 
 template <int H>
-cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st) {
+cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
   static int configured = -1;
   cudaError_t e = set_smem(fa_bwd_dq_kernel<H>, DqCfg<H>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<H><<<dim3(a.n_qtiles, a.B * a.K), kThreads, DqCfg<H>::alloc, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_qtiles * a.B * a.K);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = DqCfg<H>::alloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H>, a);
 }
 
 template <int H>
@@ -738,7 +754,7 @@ cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
   cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H>, DkvCfg<H>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<H><<<dim3(a.n_kvtiles, a.B * a.K), kThreads, DkvCfg<H>::alloc, st>>>(a);
+  fa_bwd_dkdv_kernel<H><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, DkvCfg<H>::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -784,10 +800,10 @@ cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
   }
 }
 
-cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st) {
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
   switch (a.H) {
-    case 128: return launch_dq_h<128>(a, st);
-    case 256: return launch_dq_h<256>(a, st);
+    case 128: return launch_dq_h<128>(a, st, overlap_previous);
+    case 256: return launch_dq_h<256>(a, st, overlap_previous);
     default: return cudaErrorNotSupported;
   }
 }

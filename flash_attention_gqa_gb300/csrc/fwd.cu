@@ -101,8 +101,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int Tb = kRows / a.G;                      // positions per Q tile
-  const int qt = a.n_qtiles - 1 - (int)blockIdx.x;  // heaviest (latest) tiles first
-  const int bk = blockIdx.y;
+  // Flat grid, Q-tile major: the latest (causally heaviest) Q tiles of every
+  // (batch, kv head) are dispatched first.
+  const int BKn = a.B * a.K;
+  const int qt = a.n_qtiles - 1 - (int)(blockIdx.x / BKn);
+  const int bk = (int)(blockIdx.x % BKn);
   const int b = bk / a.K;
   const int t0 = qt * Tb;
   const int n_valid = min(Tb, a.T - t0);   // positions of this tile below T
@@ -523,7 +526,7 @@ cudaError_t launch_fwd_h(const FwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(a.n_qtiles, a.B * a.K, a.n_splits);
+  dim3 grid(a.n_qtiles * a.B * a.K, 1, a.n_splits);
   fa_fwd_kernel<H><<<grid, kThreads, L::alloc, st>>>(a);
   return cudaGetLastError();
 }

@@ -67,7 +67,10 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, l
                                   cudaStream_t st);
 cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st);
-cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st);
+// overlap_previous: launch with programmatic stream serialization so the grid
+// may start while the immediately preceding dK/dV grid (which triggers its
+// dependents at start) is still running; only valid right after launch_bwd_dkdv.
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st, bool overlap_previous);
 cudaError_t launch_fill_empty(void* o, float* lse, long rows, int H, cudaStream_t st);
 cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int n_splits, void* o,
                                  float* lse, long rows, int H, cudaStream_t st);
