@@ -25,7 +25,8 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 224;  // 4 softmax-side warps, producer, two MMA issuers
+constexpr int kThreads = 224;    // dK/dV: 4 softmax-side warps, producer, two MMA issuers
+constexpr int kDqThreads = 256;  // dQ: 4 softmax-side warps, K producer, two MMA issuers, V producer
 constexpr uint32_t kQChunk = 128 * 128;  // [128 rows x 64 dims] bf16
 constexpr float kLog2e = 1.4426950408889634f;
 enum : int { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
@@ -138,7 +139,7 @@ struct DqCfg {
 };
 
 template <int H>
-__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<H>;
   constexpr int HC = C::HC, BN = C::BN, NBUF = C::NBUF, KSL = C::KSL, VSL = C::VSL;
   extern __shared__ uint8_t smem_raw[];
@@ -193,10 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
+    // K producer (and the Q / dO tiles).  K chunks are held until dQ(n) is
+    // done, V chunks only until dP(n): a separate V producer (warp 7) keeps
+    // a V load from queueing behind a K slot that is still in use.
     if (lane == 0) {
       bool ok = true;
-      uint32_t seq = 0;  // chunk sequence number, per ring (same for K and V)
-      uint32_t k_issued = 0, v_issued = 0;
+      uint32_t seq = 0;  // chunk sequence number
+      uint32_t k_issued = 0;
       bool any = false;
       for (int jt = 0; jt < jt_end && ok; ++jt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
@@ -216,6 +220,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
           tma_load_3d(sbase + C::k_off + slot * C::KV_CHUNK, &a.tm_k, kfull(slot), c * 64, jt * BN, bk);
           ++k_issued;
         }
+        seq += HC;
+      }
+      if (!ok) {
+        // Let copies in flight land before the CTA exits (bounded waits).
+        for (uint32_t sq = k_issued > KSL ? k_issued - KSL : 0; sq < k_issued; ++sq)
+          mbar_wait_teardown(kfull(sq % KSL), (sq / KSL) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 7) {
+    // V producer.
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t seq = 0, v_issued = 0;
+      for (int jt = 0; jt < jt_end && ok; ++jt) {
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = seq + c;
           const int slot = sq % VSL;
@@ -227,9 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dq_kernel(const __grid_con
         seq += HC;
       }
       if (!ok) {
-        // Let copies in flight land before the CTA exits (bounded waits).
-        for (uint32_t sq = k_issued > KSL ? k_issued - KSL : 0; sq < k_issued; ++sq)
-          mbar_wait_teardown(kfull(sq % KSL), (sq / KSL) & 1, a.wait_limit_ns);
         for (uint32_t sq = v_issued > VSL ? v_issued - VSL : 0; sq < v_issued; ++sq)
           mbar_wait_teardown(vfull(sq % VSL), (sq / VSL) & 1, a.wait_limit_ns);
       }
@@ -738,7 +754,7 @@ cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_qtiles * a.B * a.K);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kDqThreads);
   cfg.dynamicSmemBytes = DqCfg<H>::alloc;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
