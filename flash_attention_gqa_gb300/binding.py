@@ -47,6 +47,7 @@ SIGNATURES = {
     "fa_check_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "fa_set_bwd_kv_rows": (_I, [ctypes.c_int]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_sm_count": (_I, []),
 }
@@ -185,6 +186,11 @@ def fa_check_status(stream=None) -> int:
 
 def fa_set_wait_limit_ns(ns: int) -> int:
     return int(load().fa_set_wait_limit_ns(int(ns)))
+
+
+def fa_set_bwd_kv_rows(rows: int) -> int:
+    """Backward KV tile size for H = 128: 0 chooses per call, 64 / 128 force it."""
+    return int(load().fa_set_bwd_kv_rows(int(rows)))
 
 
 def fa_selftest_wait_timeout(stream=None) -> int:

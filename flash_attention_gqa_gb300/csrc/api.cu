@@ -24,6 +24,7 @@ namespace {
 using fa::kRows;
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int> g_bwd_kv_rows{0};  // 0: chosen per call; 64 / 128: forced where valid
 
 uint64_t wait_limit() {
   uint64_t v = g_wait_limit_ns.load();
@@ -277,7 +278,8 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long rows = (long)B * K * G * T;
   const int BK = B * K;
-  const int kvr = fa::bwd_kv_rows(H);
+  const int forced = g_bwd_kv_rows.load();
+  const int kvr = (H == 128 && forced != 0) ? forced : fa::bwd_kv_rows(H, B, K, S, fa_device_sm_count());
   if (BK == 0) return FA_OK;
   if (rows == 0 || S == 0) {
     // No query rows or no keys: every gradient is zero.
@@ -304,6 +306,7 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.causal = causal ? 1 : 0;
   a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
   a.n_kvtiles = (S + kvr - 1) / kvr;
+  a.kv_rows = kvr;
   a.bm = bm;
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
@@ -465,6 +468,12 @@ const char* fa_status_string(int status) {
 int fa_set_wait_limit_ns(uint64_t ns) {
   if (ns == 0) return FA_ERR_INVALID_ARG;
   g_wait_limit_ns.store(ns);
+  return FA_OK;
+}
+
+int fa_set_bwd_kv_rows(int rows) {
+  if (rows != 0 && rows != 64 && rows != 128) return FA_ERR_INVALID_ARG;
+  g_bwd_kv_rows.store(rows);
   return FA_OK;
 }
 

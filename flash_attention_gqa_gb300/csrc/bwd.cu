@@ -25,7 +25,9 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 224;    // dK/dV: 4 softmax-side warps, producer, two MMA issuers
+// dK/dV: warps 0-3 and 7-10 softmax side (two per TMEM lane quadrant, one per
+// half of the key columns), 4 producer, 5-6 MMA issuers.
+constexpr int kThreads = 352;
 constexpr int kDqThreads = 256;  // dQ: 4 softmax-side warps, K producer, two MMA issuers, V producer
 constexpr uint32_t kQChunk = 128 * 128;  // [128 rows x 64 dims] bf16
 constexpr float kLog2e = 1.4426950408889634f;
@@ -115,9 +117,9 @@ __device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, 
 }
 
 // =================================================================== dQ
-template <int H>
+template <int H, int BN_>
 struct DqCfg {
-  static constexpr int BN = bwd_kv_rows(H);            // keys per KV tile
+  static constexpr int BN = BN_;                       // keys per KV tile
   static constexpr int HC = H / 64;
   static constexpr int NBUF = (H + 4 * BN <= 512) ? 2 : 1;  // S/dP TMEM buffers
   static constexpr uint32_t KV_CHUNK = BN * 128;       // [BN rows x 64 dims]
@@ -138,9 +140,9 @@ struct DqCfg {
   __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + u * 2 * BN + BN; }
 };
 
-template <int H>
+template <int H, int BN_>
 __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
-  using C = DqCfg<H>;
+  using C = DqCfg<H, BN_>;
   constexpr int HC = C::HC, BN = C::BN, NBUF = C::NBUF, KSL = C::KSL, VSL = C::VSL;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -428,9 +430,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
 }
 
 // ================================================================ dK/dV
-template <int H>
+template <int H, int BN_>
 struct DkvCfg {
-  static constexpr int BN = bwd_kv_rows(H);   // keys per CTA
+  static constexpr int BN = BN_;              // keys per CTA
   static constexpr int HC = H / 64;
   static constexpr int HH = H / 128;          // 128-lane halves of the head dim
   static constexpr int PC = BN / 64;          // 64-key chunks of P / dS
@@ -451,9 +453,9 @@ struct DkvCfg {
   static constexpr uint32_t dp_col = 2 * HH * BN + BN;
 };
 
-template <int H>
+template <int H, int BN_>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
-  using C = DkvCfg<H>;
+  using C = DkvCfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     mbar_init(kv_full, 1);
     for (int h = 0; h < HH; ++h) { mbar_init(q_empty(h), 1); mbar_init(do_empty(h), 1); }
     mbar_init(sdp_full, 2);  // S (issuer A) and dP (issuer B)
-    mbar_init(ps_full, kRows);
+    mbar_init(ps_full, 2 * kRows);
     mbar_init(teardown(0), 1);
     mbar_init(teardown(1), 1);
     for (int c = 0; c < HC; ++c) { mbar_init(q_full(c), 1); mbar_init(do_full(c), 1); }
@@ -599,8 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       }
     }
   } else {
-    const int r = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Softmax side: the row reads TMEM lane quadrant warp % 4; the two warps of
+    // a quadrant split the key columns (no row reduction is needed: lse and D
+    // are precomputed).
+    const int quad = warp & 3, half = warp >= 7 ? 1 : 0;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    constexpr int NCH = BN / 64;  // 32-column chunks per warp
     bool ok = true;
     int i = 0;
     for (int qt = qt_begin; qt < a.n_qtiles; ++qt) {
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * NCH; c < (half + 1) * NCH; ++c) {
         uint32_t sv[32], pv[32];
         tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
         tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     for (int h = 0; h < HH; ++h) {
       const int hd = h * 128 + r;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
         uint32_t vv[32], kv[32];
         if (have) {
           tmem_ld32(tmem + lane_base + C::dv_col + h * BN + c, vv);
@@ -747,30 +754,30 @@ cudaError_t set_smem(Kern k, uint32_t bytes, int* configured) {
   return e;
 }
 
-template <int H>
+template <int H, int BN>
 cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dq_kernel<H>, DqCfg<H>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dq_kernel<H, BN>, DqCfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_qtiles * a.B * a.K);
   cfg.blockDim = dim3(kDqThreads);
-  cfg.dynamicSmemBytes = DqCfg<H>::alloc;
+  cfg.dynamicSmemBytes = DqCfg<H, BN>::alloc;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H>, a);
+  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H, BN>, a);
 }
 
-template <int H>
+template <int H, int BN>
 cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H>, DkvCfg<H>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H, BN>, DkvCfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<H><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, DkvCfg<H>::alloc, st>>>(a);
+  fa_bwd_dkdv_kernel<H, BN><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, DkvCfg<H, BN>::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -778,7 +785,7 @@ cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
 
 size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
   const size_t d = ((size_t)B * K * G * T * sizeof(float) + 255) & ~(size_t)255;
-  const size_t tb = kRows / G, kvr = bwd_kv_rows(H);
+  const size_t tb = kRows / G, kvr = kMinBwdKvRows;
   const size_t nq = (T + tb - 1) / tb, nk = (S + kvr - 1) / kvr;
   const size_t r = ((size_t)B * (nq + nk) * sizeof(int2) + 255) & ~(size_t)255;
   return d + r;
@@ -804,24 +811,22 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
   seg_ranges_kernel<<<(unsigned)((nq + warps - 1) / warps), warps * 32, 0, st>>>(a.seg_q, a.T, Tb,
                                                                                 a.n_qtiles, nq, qr);
   seg_ranges_kernel<<<(unsigned)((nk + warps - 1) / warps), warps * 32, 0, st>>>(
-      a.seg_kv, a.S, bwd_kv_rows(a.H), a.n_kvtiles, nk, kr);
+      a.seg_kv, a.S, a.kv_rows, a.n_kvtiles, nk, kr);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
-  switch (a.H) {
-    case 128: return launch_dkdv_h<128>(a, st);
-    case 256: return launch_dkdv_h<256>(a, st);
-    default: return cudaErrorNotSupported;
-  }
+  if (a.H == 128 && a.kv_rows == 128) return launch_dkdv_h<128, 128>(a, st);
+  if (a.H == 128 && a.kv_rows == 64) return launch_dkdv_h<128, 64>(a, st);
+  if (a.H == 256 && a.kv_rows == 64) return launch_dkdv_h<256, 64>(a, st);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
-  switch (a.H) {
-    case 128: return launch_dq_h<128>(a, st, overlap_previous);
-    case 256: return launch_dq_h<256>(a, st, overlap_previous);
-    default: return cudaErrorNotSupported;
-  }
+  if (a.H == 128 && a.kv_rows == 128) return launch_dq_h<128, 128>(a, st, overlap_previous);
+  if (a.H == 128 && a.kv_rows == 64) return launch_dq_h<128, 64>(a, st, overlap_previous);
+  if (a.H == 256 && a.kv_rows == 64) return launch_dq_h<256, 64>(a, st, overlap_previous);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace fa

@@ -57,6 +57,7 @@ struct BwdArgs {
   int causal;
   int n_qtiles;        // T / (128 / G)
   int n_kvtiles;       // S / kv_rows
+  int kv_rows;         // keys per KV tile of the backward kernels (64 or 128)
   BlockMask bm;
   uint32_t* err;
   uint64_t wait_limit_ns;
@@ -76,8 +77,16 @@ cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int
                                  float* lse, long rows, int H, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
-// KV rows per tile of the backward kernels for a head dim.
-constexpr int bwd_kv_rows(int H) { return H == 256 ? 64 : 128; }
+// KV rows per tile of the backward kernels.  H = 256 always takes 64 (a
+// 128-key K/V pair does not fit in shared memory next to the Q/dO tiles); H =
+// 128 takes 128 unless that leaves the dK/dV grid (one CTA per KV tile and
+// b*K) smaller than the GPU, where 64-key tiles double its CTAs.
+inline int bwd_kv_rows(int H, int B, int K, int S, int sm_count) {
+  if (H == 256) return 64;
+  const long ctas = (long)B * K * ((S + 127) / 128);
+  return ctas < sm_count ? 64 : 128;
+}
+constexpr int kMinBwdKvRows = 64;  // the workspace's range table is sized for it
 
 // Backward workspace: fp32 D rows, then per-tile segment-id ranges.
 size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H);

@@ -223,6 +223,15 @@ const char* fa_status_string(int status);
 int fa_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Keys per KV tile of the backward kernels for H = 128 calls made after this
+ * one: 0 (default) chooses per call (128, or 64 when the dK/dV grid of
+ * ceil(S/128)*B*K CTAs would not fill the GPU), 64 or 128 force that size.
+ * H = 256 always uses 64.  The result does not depend on the choice beyond
+ * fp32 summation order.  Returns FA_ERR_INVALID_ARG for any other value.
+ */
+int fa_set_bwd_kv_rows(int rows);
+
+/*
  * Self-test of the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier no one arrives on, with the current limit, and returns the status
  * fa_check_status() reports afterwards (FA_ERR_DEVICE_TIMEOUT when the

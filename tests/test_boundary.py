@@ -104,3 +104,10 @@ def test_splitkv_host_side(clib):
 def test_wait_limit_setter(clib):
     assert binding.fa_set_wait_limit_ns(0) == binding.FA_ERR_INVALID_ARG
     assert binding.fa_set_wait_limit_ns(2_000_000_000) == binding.FA_OK
+
+
+def test_bwd_kv_rows_setter(clib):
+    for bad in (-1, 1, 32, 96, 256):
+        assert binding.fa_set_bwd_kv_rows(bad) == binding.FA_ERR_INVALID_ARG
+    for ok in (64, 128, 0):
+        assert binding.fa_set_bwd_kv_rows(ok) == binding.FA_OK

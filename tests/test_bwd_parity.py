@@ -121,3 +121,34 @@ def test_h64_backward_is_rejected():
                         torch.empty_like(k), torch.empty_like(k),
                         torch.empty(4096, device=dev, dtype=torch.uint8), check=False)
     assert rc == binding.FA_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------- both KV tile sizes at H = 128
+
+@pytest.fixture
+def forced_kv_rows(request):
+    assert binding.fa_set_bwd_kv_rows(request.param) == binding.FA_OK
+    yield request.param
+    binding.fa_set_bwd_kv_rows(0)
+
+
+def _doc_segs(B, T, seed):
+    return inputs.document_segment_ids(B, T, seed=seed, lo=40, hi=300)
+
+
+KV_TILE_CASES = {
+    "causal": dict(B=1, K=2, G=4, T=384, S=384, causal=True),
+    "full_g8_ragged": dict(B=1, K=2, G=8, T=1000, S=1000, causal=False),
+    "causal_ragged": dict(B=2, K=1, G=4, T=300, S=300, causal=True),
+    "rect_causal": dict(B=2, K=2, G=4, T=100, S=300, causal=True),
+    "doc_segments": dict(B=2, K=2, G=4, T=640, S=640, causal=True, segs=True),
+}
+
+
+@pytest.mark.parametrize("forced_kv_rows", [64, 128], indirect=True)
+@pytest.mark.parametrize("name", sorted(KV_TILE_CASES))
+def test_h128_both_kv_tile_sizes(forced_kv_rows, name):
+    c = dict(KV_TILE_CASES[name])
+    seg = _doc_segs(c["B"], c["T"], 3) if c.pop("segs", False) else None
+    run_case(c["B"], c["K"], c["G"], c["T"], c["S"], 128, causal=c["causal"], seg_q=seg,
+             seg_kv=seg, seed=len(name) + forced_kv_rows)

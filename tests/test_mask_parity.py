@@ -71,3 +71,13 @@ def test_block_sparse_with_segments_and_ragged():
 
 def test_block_sparse_forward_h64_and_rectangular_causal():
     run_masked(1, 1, 4, 256, 384, 64, 4, causal=True, seed=5, backward=False)
+
+
+@pytest.mark.parametrize("rows", [64, 128])
+def test_block_sparse_h128_both_kv_tile_sizes(rows):
+    assert binding.fa_set_bwd_kv_rows(rows) == binding.FA_OK
+    try:
+        run_masked(1, 2, 4, 512, 512, 128, 8, causal=True, seed=rows)
+        run_masked(2, 2, 4, 300, 300, 128, 8, causal=True, segs=True, seed=rows + 1)
+    finally:
+        binding.fa_set_bwd_kv_rows(0)
