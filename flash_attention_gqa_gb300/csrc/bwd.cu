@@ -620,14 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
       const float Dr = valid ? a.delta[row] : 0.f;
       const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
+      // sdp_full completes through a tcgen05.commit of each issuer after S(i) /
+      // dP(i), which tracks every earlier product of that issuer too: the
+      // previous tile's dK^T / dV^T, the readers of the P and dS buffers, are
+      // done, so the buffers may be overwritten.
       if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
-      // P and dS shared buffers are free once the previous tile's dV^T and dK^T
-      // are done (the last half's release barriers follow every earlier product).
-      if (i > 0 && (!warp_wait(q_empty(HH - 1), (i - 1) & 1, ab) ||
-                    !warp_wait(do_empty(HH - 1), (i - 1) & 1, ab))) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
 #pragma unroll 1
       for (int c = half * NCH; c < (half + 1) * NCH; ++c) {
