@@ -116,6 +116,18 @@ __device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, 
   }
 }
 
+// Row r, key columns [32c, 32c + 32) (16 bf16 pairs) into a [128 rows x BN keys]
+// operand stored as [128 x 64] chunks with the 128-byte swizzle: 16-byte unit u
+// of a row lands at unit u ^ (r % 8).
+__device__ __forceinline__ void store_row32(uint8_t* base, int r, int c, const uint32_t* w) {
+  const int chunk = (c * 32) / 64, u0 = ((c * 32) % 64) / 8;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t off = chunk * kQChunk + r * 128 + (((u0 + k) ^ (r & 7)) * 16);
+    *reinterpret_cast<uint4*>(base + off) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
 // =================================================================== dQ
 template <int H, int BN_>
 struct DqCfg {
@@ -444,8 +456,9 @@ struct DkvCfg {
   static constexpr uint32_t p_off = do_off + HC * kQChunk;
   static constexpr uint32_t ds_off = p_off + PC * kQChunk;
   static constexpr uint32_t bar_off = ds_off + PC * kQChunk;
-  // kv_full, sdp_full, ps_full, teardown[2], q_full[HC], do_full[HC], q_empty[HH], do_empty[HH]
-  static constexpr uint32_t misc_off = bar_off + (5 + 2 * HC + 2 * HH) * 8;
+  // kv_full, s_full, dp_full, p_full, ds_full, teardown[2], q_full[HC], do_full[HC],
+  // q_empty[HH], do_empty[HH]
+  static constexpr uint32_t misc_off = bar_off + (7 + 2 * HC + 2 * HH) * 8;
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
   static constexpr uint32_t dv_col = 0;
   static constexpr uint32_t dk_col = HH * BN;
@@ -462,13 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar0 = sbase + C::bar_off;
-  const uint32_t kv_full = bar0, sdp_full = bar0 + 8, ps_full = bar0 + 16;
-  auto teardown = [&](int i) { return bar0 + 8 * (3 + i); };
-  auto q_full = [&](int c) { return bar0 + 8 * (5 + c); };
-  auto do_full = [&](int c) { return bar0 + 8 * (5 + HC + c); };
+  const uint32_t kv_full = bar0, s_full = bar0 + 8, dp_full = bar0 + 16;
+  const uint32_t p_full = bar0 + 24, ds_full = bar0 + 32;
+  auto teardown = [&](int i) { return bar0 + 8 * (5 + i); };
+  auto q_full = [&](int c) { return bar0 + 8 * (7 + c); };
+  auto do_full = [&](int c) { return bar0 + 8 * (7 + HC + c); };
   // Q (dO) 128-dim half h is released once dK^T (dV^T) of that half is done.
-  auto q_empty = [&](int h) { return bar0 + 8 * (5 + 2 * HC + h); };
-  auto do_empty = [&](int h) { return bar0 + 8 * (5 + 2 * HC + HH + h); };
+  auto q_empty = [&](int h) { return bar0 + 8 * (7 + 2 * HC + h); };
+  auto do_empty = [&](int h) { return bar0 + 8 * (7 + 2 * HC + HH + h); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
   const Abort ab{abort_flag, a.wait_limit_ns, a.err};
@@ -491,8 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     *abort_flag = 0;
     mbar_init(kv_full, 1);
     for (int h = 0; h < HH; ++h) { mbar_init(q_empty(h), 1); mbar_init(do_empty(h), 1); }
-    mbar_init(sdp_full, 2);  // S (issuer A) and dP (issuer B)
-    mbar_init(ps_full, 2 * kRows);
+    mbar_init(s_full, 1);           // S done (issuer A's commit)
+    mbar_init(dp_full, 1);          // dP done (issuer B's commit)
+    mbar_init(p_full, 2 * kRows);   // P written (softmax side)
+    mbar_init(ds_full, 2 * kRows);  // dS written (softmax side)
     mbar_init(teardown(0), 1);
     mbar_init(teardown(1), 1);
     for (int c = 0; c < HC; ++c) { mbar_init(q_full(c), 1); mbar_init(do_full(c), 1); }
@@ -551,6 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   } else if (warp == 5 || warp == 6) {
     // Two MMA issuers: A (warp 5) issues S = Q K^T and dK^T += Q^T dS (the Q
     // operand), B (warp 6) issues dP = dO V^T and dV^T += dO^T P (the dO operand).
+    // P needs only S, so dV^T(i) starts while the softmax side still computes
+    // dS(i) = P (dP - D); dK^T(i) follows once dS(i) is written.
     if (lane == 0) {
       const bool is_a = warp == 5;
       constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);  // S, dP: [128 q x BN]
@@ -570,8 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
-        // This issuer's S (or dP) columns of the previous tile were read before
-        // the softmax side signalled ps_full, which it waited for below.
+        // S(i-1) was read before P(i-1) was signalled, and A waited for dS(i-1),
+        // later still; dP(i-1) is read until dS(i-1) is signalled, so B waits here.
+        if (!is_a && i > 0 && !mbar_wait(ds_full, (i - 1) & 1, ab)) { ok = false; break; }
         for (int c = 0; c < HC && ok; ++c) {
           if (!mbar_wait(is_a ? q_full(c) : do_full(c), i & 1, ab)) { ok = false; break; }
           tc_fence_after();
@@ -582,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
                    (c > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(sdp_full);
-        if (!mbar_wait(ps_full, i & 1, ab)) { ok = false; break; }
+        mma_commit(is_a ? s_full : dp_full);
+        if (!mbar_wait(is_a ? ds_full : p_full, i & 1, ab)) { ok = false; break; }
         tc_fence_after();
         for (int h = 0; h < HH; ++h) {  // contraction over the 128 packed query rows
           const uint64_t xA = sdesc_add(d_xT, 2 * h * kQChunk);
@@ -620,42 +639,50 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
       const float Dr = valid ? a.delta[row] : 0.f;
       const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
-      // sdp_full completes through a tcgen05.commit of each issuer after S(i) /
-      // dP(i), which tracks every earlier product of that issuer too: the
-      // previous tile's dK^T / dV^T, the readers of the P and dS buffers, are
-      // done, so the buffers may be overwritten.
-      if (!warp_wait(sdp_full, i & 1, ab)) { ok = false; break; }
+      // Phase 1: P = exp(S - lse) once S(i) is done.  s_full is A's commit, which
+      // also covers dK^T(i-1) (the reader of the dS buffer); the P buffer's
+      // reader dV^T(i-1) is B's, so its release barrier is waited for here.
+      if (!warp_wait(s_full, i & 1, ab)) { ok = false; break; }
+      if (i > 0 && !warp_wait(do_empty(HH - 1), (i - 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = half * NCH; c < (half + 1) * NCH; ++c) {
-        uint32_t sv[32], pv[32];
+      uint32_t pp[NCH][16];  // this warp's P (bf16 pairs), kept for phase 2
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;
+        uint32_t sv[32];
         tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
-        tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
         tmem_wait_ld();
-        float* s = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
-        uint32_t pp[16], dd[16];
+        float* sf = reinterpret_cast<float*>(sv);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float p0 = fast_exp2(fmaf(s[2 * k], kLog2e, -lse2));
-          const float p1 = fast_exp2(fmaf(s[2 * k + 1], kLog2e, -lse2));
-          pp[k] = pack_bf16x2(p0, p1);
-          dd[k] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * k]) - Dr), p1 * (__uint_as_float(pv[2 * k + 1]) - Dr));
-        }
-        // Row r of the [128 q x 64 key] chunk, 128-byte swizzle: 16-byte unit u
-        // of the row lands at unit u ^ (r % 8).
-        const int chunk = (c * 32) / 64;
-        const int u0 = ((c * 32) % 64) / 8;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t off = chunk * kQChunk + r * 128 + (((u0 + k) ^ (r & 7)) * 16);
-          *reinterpret_cast<uint4*>(sm + C::p_off + off) = *reinterpret_cast<uint4*>(&pp[4 * k]);
-          *reinterpret_cast<uint4*>(sm + C::ds_off + off) = *reinterpret_cast<uint4*>(&dd[4 * k]);
-        }
+        for (int k = 0; k < 16; ++k)
+          pp[cc][k] = pack_bf16x2(fast_exp2(fmaf(sf[2 * k], kLog2e, -lse2)),
+                                  fast_exp2(fmaf(sf[2 * k + 1], kLog2e, -lse2)));
+        store_row32(sm + C::p_off, r, c, pp[cc]);
       }
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor cores
       tc_fence_before();
-      mbar_arrive(ps_full);
+      mbar_arrive(p_full);
+      // Phase 2: dS = P (dP - D) once dP(i) is done (masked entries have P = 0).
+      if (!warp_wait(dp_full, i & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;
+        uint32_t pv[32], dd[16];
+        tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 pk = unpack_bf16x2(pp[cc][k]);
+          dd[k] = pack_bf16x2(pk.x * (__uint_as_float(pv[2 * k]) - Dr),
+                              pk.y * (__uint_as_float(pv[2 * k + 1]) - Dr));
+        }
+        store_row32(sm + C::ds_off, r, c, dd);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
       ++i;
     }
     // Epilogue: lanes carry the head dim, columns the keys.
