@@ -720,20 +720,37 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
 }
 
-// D[row] = sum_h dO[row, h] * o[row, h] in fp32; one warp per row.
+// D[row] = sum_h dO[row, h] * o[row, h] in fp32.  H / 8 lanes share a row
+// (one 16-byte load of o and of dO each); a warp covers 32 / (H / 8) rows per
+// step and takes kPreSteps steps with all loads issued before any is used, so
+// each warp keeps 2 * kPreSteps loads in flight.  HBM-bound.
+constexpr int kPreSteps = 4;
+template <int H>
 __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                       const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
-                                      long rows, int H) {
-  const long row = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+                                      long rows) {
+  constexpr int TPR = H / 8, RPW = 32 / TPR;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint4* po = reinterpret_cast<const uint4*>(o + row * H);
-  const uint4* pd = reinterpret_cast<const uint4*>(dO + row * H);
-  float acc = 0.f;
-  for (int i = lane; i < H / 8; i += 32) {
-    const uint4 x = __ldg(po + i), d = __ldg(pd + i);
-    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&x);
-    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
+  const long warp_id = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const long row0 = warp_id * kPreSteps * RPW + lane / TPR;
+  const int col = lane % TPR;
+  uint4 x[kPreSteps], d[kPreSteps];
+#pragma unroll
+  for (int u = 0; u < kPreSteps; ++u) {
+    const long row = row0 + (long)u * RPW;
+    if (row < rows) {
+      x[u] = __ldg(reinterpret_cast<const uint4*>(o + row * H) + col);
+      d[u] = __ldg(reinterpret_cast<const uint4*>(dO + row * H) + col);
+    } else {
+      x[u] = make_uint4(0, 0, 0, 0);
+      d[u] = make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPreSteps; ++u) {
+    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d[u]);
+    float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 fx = __bfloat1622float2(x2[j]);
@@ -741,10 +758,11 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
       acc = fmaf(fx.x, fd.x, acc);
       acc = fmaf(fx.y, fd.y, acc);
     }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) delta[row] = acc;
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const long row = row0 + (long)u * RPW;
+    if (col == 0 && row < rows) delta[row] = acc;
+  }
 }
 
 // Per-tile [min, max] of segment ids: one warp per (b, tile).
@@ -818,10 +836,18 @@ size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
                                   cudaStream_t st) {
   const int warps = 8;
-  const long blocks = (rows + warps - 1) / warps;
-  bwd_preprocess_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dO), delta,
-      rows, H);
+  auto go = [&](auto kern, int tpr) {
+    const long rows_per_block = (long)warps * kPreSteps * (32 / tpr);
+    const long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    kern<<<(unsigned)blocks, warps * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(o),
+                                                  reinterpret_cast<const __nv_bfloat16*>(dO), delta,
+                                                  rows);
+  };
+  switch (H) {
+    case 128: go(bwd_preprocess_kernel<128>, 16); break;
+    case 256: go(bwd_preprocess_kernel<256>, 32); break;
+    default: return cudaErrorNotSupported;
+  }
   return cudaGetLastError();
 }
 
