@@ -128,6 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     mbar_init(bars.teardown(), 1);
     fence_barrier_init();
+    // Every CTA with work needs its Q tile: start the copy before the
+    // schedule is built, so its latency overlaps the tile classification.
+    mbar_arrive_expect_tx(bars.q_full(), HC * kChunkBytes);
+    for (int c = 0; c < HC; ++c)
+      tma_load_4d(sbase + L::q_off + c * kChunkBytes, &a.tm_q, bars.q_full(), c * 64, t0, 0, bk);
   }
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -216,9 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_tiles > 0) {
-      mbar_arrive_expect_tx(bars.q_full(), HC * kChunkBytes);
-      for (int c = 0; c < HC; ++c)
-        tma_load_4d(sbase + L::q_off + c * kChunkBytes, &a.tm_q, bars.q_full(), c * 64, t0, 0, bk);
       uint32_t seq = 0;
       bool ok = true;
       for (int u = 0; u < 2 * n_tiles && ok; ++u) {
@@ -485,6 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
   }
 
+  // The Q copy started at entry must have landed before the CTA exits (it
+  // has unless this CTA had no tiles or gave up waiting).
+  if (tid == 0) mbar_wait_teardown(bars.q_full(), 0, a.wait_limit_ns);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
