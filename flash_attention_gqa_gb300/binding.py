@@ -48,6 +48,7 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "fa_set_bwd_kv_rows": (_I, [ctypes.c_int]),
+    "fa_set_fwd_schedule": (_I, [ctypes.c_int]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_sm_count": (_I, []),
 }
@@ -186,6 +187,11 @@ def fa_check_status(stream=None) -> int:
 
 def fa_set_wait_limit_ns(ns: int) -> int:
     return int(load().fa_set_wait_limit_ns(int(ns)))
+
+
+def fa_set_fwd_schedule(mode: int) -> int:
+    """Forward grid: 0 chooses, 1 one CTA per Q tile, 2 persistent (H <= 128, no split-KV)."""
+    return int(load().fa_set_fwd_schedule(int(mode)))
 
 
 def fa_set_bwd_kv_rows(rows: int) -> int:

@@ -25,6 +25,7 @@ using fa::kRows;
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_bwd_kv_rows{0};  // 0: chosen per call; 64 / 128: forced where valid
+std::atomic<int> g_fwd_schedule{0};  // 0: chosen per call; 1: CTA per Q tile; 2: persistent
 
 uint64_t wait_limit() {
   uint64_t v = g_wait_limit_ns.load();
@@ -188,7 +189,7 @@ int fwd_common(const void* q, const void* k, const void* v, const int32_t* seg_q
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
-  cudaError_t e = fa::launch_fwd(a, st);
+  cudaError_t e = fa::launch_fwd(a, st, g_fwd_schedule.load());
   if (e == cudaSuccess && n_splits > 1)
     e = fa::launch_split_combine(a.part_o, a.part_lse, n_splits, o, lse, rows, H, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -474,6 +475,12 @@ int fa_set_wait_limit_ns(uint64_t ns) {
 int fa_set_bwd_kv_rows(int rows) {
   if (rows != 0 && rows != 64 && rows != 128) return FA_ERR_INVALID_ARG;
   g_bwd_kv_rows.store(rows);
+  return FA_OK;
+}
+
+int fa_set_fwd_schedule(int mode) {
+  if (mode < 0 || mode > 2) return FA_ERR_INVALID_ARG;
+  g_fwd_schedule.store(mode);
   return FA_OK;
 }
 

@@ -79,6 +79,152 @@ __device__ __forceinline__ uint32_t unit_v(int n, int n_tiles) {
 // Tile classes of the lazy mask.
 enum : uint8_t { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
 
+// One KV tile of the online softmax for packed row r (TMEM lane r): wait for
+// S(N) (global tile counter N: buffer N & 1), apply the lazy mask on PARTIAL
+// tiles, update the running max m_ref / denominator l (rescaling O, after
+// O += P V of tile N - 1, only when m moved by more than 2^8), write P (bf16)
+// over the first 64 columns of the S buffer and signal p_full.  n is the tile's
+// index within its Q tile (n == 0 starts the row).  O lives in TMEM columns
+// [o_col, o_col + H).  Returns false when a bounded wait gave up.
+template <int H>
+__device__ __forceinline__ bool softmax_tile(const FwdArgs& a, uint32_t tmem, uint32_t lane_base,
+                                             uint16_t entry, int n, int N, int t, int g, bool valid,
+                                             int my_seg, int b, int kh, const Bars& bars,
+                                             const Abort& ab, float& m_ref, float& l,
+                                             uint32_t o_col = 0) {
+  const int j = entry & 0x7fff;
+  const bool partial = (entry & 0x8000) != 0;
+  const int off = a.S - a.T;
+  const bool segs = a.seg_q != nullptr;
+  if (!warp_wait(bars.s_full(N & 1), (N >> 1) & 1, ab)) return false;
+  tc_fence_after();
+  const uint32_t s_col = 256 + 128 * (N & 1);
+  uint32_t sv[4][32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + s_col + c * 32, sv[c]);
+  tmem_wait_ld();
+  float* s = reinterpret_cast<float*>(&sv[0][0]);
+  if (partial) {
+    const int s0 = j * kKvRows;
+    const int lim = a.causal ? min(t + off, a.S - 1) : a.S - 1;  // last key kept
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (s0 + c > lim) s[c] = -INFINITY;
+    if (segs) {
+      // every thread reads the same 512 B of key ids: served by L1 broadcast
+      const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
+      if ((a.S & 3) == 0 && s0 + 128 <= a.S) {  // aligned and in range
+        const int4* kid = reinterpret_cast<const int4*>(ids);
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4) {
+          const int4 v = __ldg(kid + c4);
+          if (v.x != my_seg) s[4 * c4 + 0] = -INFINITY;
+          if (v.y != my_seg) s[4 * c4 + 1] = -INFINITY;
+          if (v.z != my_seg) s[4 * c4 + 2] = -INFINITY;
+          if (v.w != my_seg) s[4 * c4 + 3] = -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (s0 + c < a.S && __ldg(ids + c) != my_seg) s[c] = -INFINITY;
+      }
+    }
+    if (a.bm.cls != nullptr && valid) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t bits = bm_row_word(a.bm, kh, a.G, g, t, j, w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (!((bits >> i) & 1u)) s[32 * w + i] = -INFINITY;
+      }
+    }
+  }
+  // Row max with 8 independent partial maxima (short dependency chains).
+  float pm[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pm[i] = s[i];
+#pragma unroll
+  for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pm[i] = fmaxf(pm[i], s[c + i]);
+  }
+  const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                         fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+  const float m_tile = mx * kLog2e;
+  float alpha = 1.f;
+  bool rescale = false;
+  if (n == 0) {
+    m_ref = m_tile;
+  } else if (m_tile > m_ref + kRescaleThreshold) {
+    alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_tile);
+    m_ref = m_tile;
+    rescale = true;
+  }
+  const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+  // O must be rescaled before O += P V of this tile; it holds every earlier tile.
+  if (__any_sync(0xffffffffu, rescale)) {
+    if (!warp_wait(bars.pv_done((N - 1) & 1), ((N - 1) >> 1) & 1, ab)) return false;
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < H; c += 32) {
+      uint32_t ov[32];
+      tmem_ld32(tmem + lane_base + o_col + c, ov);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+      tmem_st32(tmem + lane_base + o_col + c, ov);
+    }
+  }
+  // P = exp2(S log2e - m) in two halves of 64 keys; bf16 pairs overwrite the
+  // first 64 columns of this tile's S buffer (already read into registers).
+  float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float p0 = fast_exp2(fmaf(s[64 * hf + 2 * c], kLog2e, -m_use));
+      const float p1 = fast_exp2(fmaf(s[64 * hf + 2 * c + 1], kLog2e, -m_use));
+      ps[c & 3] += p0 + p1;
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tmem + lane_base + s_col + 32 * hf, pk);
+  }
+  l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(bars.p_full(N & 1));
+  return true;
+}
+
+// O / l of packed row r in bf16 into a Q-shaped shared-memory tile (H/64
+// chunks of [128 rows x 128 B], 128-byte swizzle), ready for TMA stores.  O is
+// read from TMEM columns [o_col, o_col + H) when `have`, else zeros are written.
+template <int H>
+__device__ __forceinline__ void stage_o_row(uint8_t* q_tile, uint32_t tmem, uint32_t lane_base,
+                                            uint32_t o_col, int r, bool have, float inv) {
+#pragma unroll 1
+  for (int c = 0; c < H; c += 32) {
+    uint32_t ov[32];
+    if (have) {
+      tmem_ld32(tmem + lane_base + o_col + c, ov);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = 0;
+    }
+    uint4 pkd[4];
+    uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+    uint8_t* chunk = q_tile + (c / 64) * kChunkBytes;
+    const uint32_t u0 = (c % 64) / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
+  }
+}
+
 template <int H>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdSmem<H>;
@@ -319,106 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     float l = 0.f;            // running denominator (relative to m_ref)
     bool ok = true;
     for (int n = 0; n < n_tiles; ++n) {
-      const int j = sched[n] & 0x7fff;
-      const bool partial = (sched[n] & 0x8000) != 0;
-      if (!warp_wait(bars.s_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t s_col = 256 + 128 * (n & 1);
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + s_col + c * 32, sv[c]);
-      tmem_wait_ld();
-      float* s = reinterpret_cast<float*>(&sv[0][0]);
-      if (partial) {
-        const int s0 = j * kKvRows;
-        const int lim = a.causal ? min(t + off, a.S - 1) : a.S - 1;  // last key kept
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (s0 + c > lim) s[c] = -INFINITY;
-        if (segs) {
-          // every thread reads the same 512 B of key ids: served by L1 broadcast
-          const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
-          if ((a.S & 3) == 0 && s0 + 128 <= a.S) {  // aligned and in range
-            const int4* kid = reinterpret_cast<const int4*>(ids);
-#pragma unroll
-            for (int c4 = 0; c4 < 32; ++c4) {
-              const int4 v = __ldg(kid + c4);
-              if (v.x != my_seg) s[4 * c4 + 0] = -INFINITY;
-              if (v.y != my_seg) s[4 * c4 + 1] = -INFINITY;
-              if (v.z != my_seg) s[4 * c4 + 2] = -INFINITY;
-              if (v.w != my_seg) s[4 * c4 + 3] = -INFINITY;
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (s0 + c < a.S && __ldg(ids + c) != my_seg) s[c] = -INFINITY;
-          }
-        }
-        if (a.bm.cls != nullptr && valid) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t bits = bm_row_word(a.bm, bk % a.K, a.G, g, t, j, w);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (!((bits >> i) & 1u)) s[32 * w + i] = -INFINITY;
-          }
-        }
+      if (!softmax_tile<H>(a, tmem, lane_base, sched[n], n, n, t, g, valid, my_seg, b, bk % a.K,
+                           bars, ab, m_ref, l)) {
+        ok = false;
+        break;
       }
-      // Row max with 8 independent partial maxima (short dependency chains).
-      float pm[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pm[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < 128; c += 8) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pm[i] = fmaxf(pm[i], s[c + i]);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      const float m_tile = mx * kLog2e;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (n == 0) {
-        m_ref = m_tile;
-      } else if (m_tile > m_ref + kRescaleThreshold) {
-        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_tile);
-        m_ref = m_tile;
-        rescale = true;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // O must be rescaled before O += P V of this tile; it holds every earlier tile.
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!warp_wait(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < H; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + c, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(tmem + lane_base + c, ov);
-        }
-      }
-      // P = exp2(S log2e - m) in two halves of 64 keys; bf16 pairs overwrite the
-      // first 64 columns of this tile's S buffer (already read into registers).
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(fmaf(s[64 * hf + 2 * c], kLog2e, -m_use));
-          const float p1 = fast_exp2(fmaf(s[64 * hf + 2 * c + 1], kLog2e, -m_use));
-          ps[c & 3] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tmem + lane_base + s_col + 32 * hf, pk);
-      }
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_full(n & 1));
     }
     // ------------------------------------------------------------ epilogue
     // O / l in bf16 is staged in the Q tile's shared memory (free: every MMA
@@ -455,26 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
       if (valid) a.part_lse[prow] = lse_row;
     } else {
-#pragma unroll 1
-      for (int c = 0; c < H; c += 32) {
-        uint32_t ov[32];
-        if (have) {
-          tmem_ld32(tmem + lane_base + c, ov);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = 0;
-        }
-        uint4 pkd[4];
-        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-        uint8_t* chunk = sm + L::q_off + (c / 64) * kChunkBytes;
-        const uint32_t u0 = (c % 64) / 8;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pkd[i];
-      }
+      stage_o_row<H>(sm + L::q_off, tmem, lane_base, 0, r, have, inv);
       if (valid) a.lse[row] = lse_row;
       fence_proxy_async_smem();
       named_bar_sync(1, kRows);
@@ -490,6 +522,358 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // The Q copy started at entry must have landed before the CTA exits (it
   // has unless this CTA had no tiles or gave up waiting).
   if (tid == 0) mbar_wait_teardown(bars.q_full(), 0, a.wait_limit_ns);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Persistent forward for H <= 128 without split-KV.  One CTA per SM walks the
+// LPT-ordered Q tiles (items) blockIdx.x, blockIdx.x + gridDim.x, ...  The Q
+// tile, the KV-tile schedule and the O accumulator of an item are double
+// buffered (b = local item index & 1), so a scheduler warp classifies the KV
+// tiles of item k+1 and starts its Q copy while item k runs, and the MMA warp
+// computes the first S tiles of item k+1 while the softmax warps finish item
+// k's epilogue.  Roles (224 threads): warps 0-3 softmax and epilogue, warp 4
+// K/V producer, warp 5 MMA issuer and TMEM owner, warp 6 scheduler.  Tensor
+// memory: O[b] at columns [128 b, 128 b + H), S buffers at 256 and 384.
+constexpr int kPThreads = 224;
+
+template <int H>
+struct PFwdSmem {
+  static constexpr int HC = H / 64;
+  static constexpr uint32_t q_off = 0;  // Q[b] at q_off + b * HC * kChunkBytes
+  static constexpr uint32_t ring_off = 2 * HC * kChunkBytes;
+  static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[2][kMaxKvTiles]
+  static constexpr uint32_t bar_off = sched_off + 2 * kMaxKvTiles * 2;
+  // q_full[2], sched_full[2], item_free[2], then the Bars block (full, empty,
+  // s_full, p_full, pv_done, teardown)
+  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, item info[2][4]
+  static constexpr uint32_t bytes = misc_off + 64;
+  static constexpr uint32_t alloc = bytes + 1024;
+};
+
+template <int H>
+__global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const __grid_constant__ FwdArgs a) {
+  using L = PFwdSmem<H>;
+  constexpr int HC = L::HC;
+  static_assert(H <= 128, "two O accumulators must fit next to the S buffers");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t pb = sbase + L::bar_off;
+  auto q_full = [&](int b) { return pb + 8 * b; };
+  auto sched_full = [&](int b) { return pb + 8 * (2 + b); };
+  auto item_free = [&](int b) { return pb + 8 * (4 + b); };
+  Bars bars{pb + 8 * 6};
+  auto sched = [&](int b) { return reinterpret_cast<uint16_t*>(sm + L::sched_off) + b * kMaxKvTiles; };
+  auto q_tile = [&](int b) { return L::q_off + (uint32_t)b * HC * kChunkBytes; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc_off + 4);
+  volatile int* info_all = reinterpret_cast<volatile int*>(sm + L::misc_off + 16);  // [2][4]
+  const Abort ab{abort_flag, a.wait_limit_ns, a.err};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Tb = kRows / a.G;
+  const int BKn = a.B * a.K;
+  const int n_items = a.n_qtiles * BKn;
+  const int off = a.S - a.T;
+  const int n_kv_all = (a.S + kKvRows - 1) / kKvRows;
+  const bool segs = a.seg_q != nullptr;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(q_full(b), 1);
+      mbar_init(sched_full(b), 1);
+      // producer done with the schedule, MMA warp has read the tile count,
+      // epilogue stored: the item's buffers may be refilled
+      mbar_init(item_free(b), 3);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full(i), 1);
+      mbar_init(bars.p_full(i), kRows);
+      mbar_init(bars.pv_done(i), 1);
+    }
+    mbar_init(bars.teardown(), 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
+  if (warp == 4) { prefetch_tmap(&a.tm_k); prefetch_tmap(&a.tm_v); }
+  if (warp == 6) { prefetch_tmap(&a.tm_q); prefetch_tmap(&a.tm_o); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 6) {
+    // ---------------------------------------------------------- scheduler
+    bool ok = true;
+    int k = 0;
+    for (;; ++k) {
+      const int b = k & 1;
+      // buffers b were last used by item k - 2
+      if (k >= 2 && !warp_wait(item_free(b), ((k >> 1) - 1) & 1, ab)) { ok = false; break; }
+      volatile int* info = info_all + 4 * b;
+      // Snake order over the LPT list: even rounds left to right, odd rounds
+      // right to left, so every CTA's share of the decreasing sizes evens out.
+      const int G = (int)gridDim.x;
+      const int item = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+      if (item >= n_items) {
+        if (lane == 0) { info[0] = -1; mbar_arrive(sched_full(b)); }
+        break;
+      }
+      const int qt = a.n_qtiles - 1 - item / BKn, bk = item % BKn, bb = bk / a.K;
+      const int t0 = qt * Tb, n_valid = min(Tb, a.T - t0);
+      int n_kv = n_kv_all;
+      if (a.causal) {
+        const int lim = t0 + n_valid - 1 + off;
+        n_kv = lim < 0 ? 0 : min(n_kv_all, lim / kKvRows + 1);
+      }
+      int qmn = INT_MAX, qmx = INT_MIN;
+      if (segs) {
+        for (int i = lane; i < n_valid; i += 32) {
+          const int v = a.seg_q[(long)bb * a.T + t0 + i];
+          qmn = min(qmn, v);
+          qmx = max(qmx, v);
+        }
+        qmn = __reduce_min_sync(0xffffffffu, qmn);
+        qmx = __reduce_max_sync(0xffffffffu, qmx);
+      }
+      // Classify 32 KV tiles at a time, one per lane, and compact the
+      // non-empty ones (ballot prefix sums) into the schedule.
+      uint16_t* list = sched(b);
+      int count = 0;
+      for (int j0 = 0; j0 < n_kv; j0 += 32) {
+        const int j = j0 + lane;
+        uint8_t c = TILE_EMPTY;
+        if (j < n_kv) {
+          c = TILE_FULL;
+          const int s_first = j * kKvRows, s_last = min(s_first + kKvRows, a.S) - 1;
+          if (a.causal && s_last > t0 + off) c = TILE_PARTIAL;  // crosses the diagonal
+          if (s_first + kKvRows > a.S) c = TILE_PARTIAL;         // ragged last tile
+          if (segs) {
+            int mn = INT_MAX, mx = INT_MIN;
+            const int32_t* ids = a.seg_kv + (long)bb * a.S + s_first;
+            if ((a.S & 3) == 0 && s_first + kKvRows <= a.S) {
+              const int4* kid = reinterpret_cast<const int4*>(ids);
+#pragma unroll 8
+              for (int e = 0; e < kKvRows / 4; ++e) {
+                const int4 v = __ldg(kid + e);
+                mn = min(min(mn, v.x), min(v.y, min(v.z, v.w)));
+                mx = max(max(mx, v.x), max(v.y, max(v.z, v.w)));
+              }
+            } else {
+              for (int e = 0; e <= s_last - s_first; ++e) {
+                const int v = __ldg(ids + e);
+                mn = min(mn, v);
+                mx = max(mx, v);
+              }
+            }
+            if (mx < qmn || mn > qmx) c = TILE_EMPTY;
+            else if (!(mn == mx && qmn == qmx && mn == qmn)) c = TILE_PARTIAL;
+          }
+          if (c != TILE_EMPTY && a.bm.cls != nullptr)  // the Q tile lies inside one 128-position block
+            c = (uint8_t)class_and(c, bm_tile_class(a.bm, bk % a.K, a.G, t0 >> 7, j));
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, c != TILE_EMPTY);
+        if (c != TILE_EMPTY)
+          list[count + __popc(m & ((1u << lane) - 1))] = (uint16_t)(j | (c == TILE_PARTIAL ? 0x8000 : 0));
+        count += __popc(m);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        info[0] = count; info[1] = qt; info[2] = bk;
+        if (count > 0) {
+          mbar_arrive_expect_tx(q_full(b), HC * kChunkBytes);
+          for (int c = 0; c < HC; ++c)
+            tma_load_4d(sbase + q_tile(b) + c * kChunkBytes, &a.tm_q, q_full(b), c * 64, t0, 0, bk);
+        } else {
+          mbar_arrive(q_full(b));  // keep the phase count of q_full(b) in step
+        }
+        mbar_arrive(sched_full(b));
+      }
+    }
+    // Q copies still in flight (the last two items) land before the CTA exits.
+    if (lane == 0) {
+      for (int kk = max(0, k - 2); kk < k; ++kk)
+        mbar_wait_teardown(q_full(kk & 1), (kk >> 1) & 1, a.wait_limit_ns);
+    }
+    (void)ok;
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t seq = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int b = k & 1;
+        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
+        volatile int* info = info_all + 4 * b;
+        const int n_tiles = info[0];
+        if (n_tiles < 0) break;
+        const int bk = info[2];
+        const uint16_t* list = sched(b);
+        for (int u = 0; u < 2 * n_tiles && ok; ++u) {
+          // unit 0: K(0); last unit: V(N-1); odd u: K((u+1)/2); even u: V(u/2 - 1)
+          bool is_k;
+          int n;
+          if (u == 0) { is_k = true; n = 0; }
+          else if (u == 2 * n_tiles - 1) { is_k = false; n = n_tiles - 1; }
+          else if (u & 1) { is_k = true; n = (u + 1) / 2; }
+          else { is_k = false; n = u / 2 - 1; }
+          const int j = list[n] & 0x7fff;
+          const CUtensorMap* m = is_k ? &a.tm_k : &a.tm_v;
+          for (int c = 0; c < HC; ++c, ++seq) {
+            const int slot = seq % kSlots;
+            if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
+            tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
+                        j * kKvRows, bk);
+          }
+        }
+        if (ok) mbar_arrive(item_free(b));  // done with this item's schedule
+      }
+      if (!ok) {
+        const uint32_t first = seq > kSlots ? seq - kSlots : 0;
+        for (uint32_t q = first; q < seq; ++q)
+          mbar_wait_teardown(bars.full(q % kSlots), (q / kSlots) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
+      constexpr uint32_t id_o = idesc_bf16(128, H, false, true);     // O += P V (N = H)
+      const uint64_t dk0 = sdesc_sw128(sbase + L::ring_off, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + L::ring_off, kChunkBytes, 1024);
+      bool ok = true;
+      uint32_t seq_base = 0;  // ring chunks of earlier items
+      int N = 0;              // tiles of earlier items (S / P buffer and parity counter)
+      for (int k = 0; ok; ++k) {
+        const int b = k & 1;
+        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
+        const int n_tiles = info_all[4 * b];
+        if (n_tiles < 0) break;
+        // Nothing else of the item's shared state is read here (O[b] and Q[b]
+        // are released by the epilogue, which waits for this warp's products).
+        mbar_arrive(item_free(b));
+        if (n_tiles == 0) continue;
+        if (!mbar_wait(q_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
+        const uint64_t dq0 = sdesc_sw128(sbase + q_tile(b), 16, 1024);
+        const uint32_t o_col = 128u * b;
+        auto issue_pv = [&](int n) -> bool {
+          const int Nn = N + n;
+          if (!mbar_wait(bars.p_full(Nn & 1), (Nn >> 1) & 1, ab)) return false;
+          const uint32_t seq0 = seq_base + unit_v(n, n_tiles) * HC;
+          const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
+          for (int c = 0; c < HC; ++c)
+            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) return false;
+          tc_fence_after();
+          const uint32_t p_col = 256 + 128 * (Nn & 1);
+          const uint64_t bv = sdesc_add(dv0, slot0 * kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKvRows / 16; ++kk)
+            mma_ts(tmem + o_col, tmem + p_col + kk * 8, sdesc_add(bv, kk * 2048), id_o,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < HC; ++c) mma_commit(bars.empty(slot0 + c));
+          mma_commit(bars.pv_done(Nn & 1));
+          return true;
+        };
+        for (int n = 0; n < n_tiles && ok; ++n) {
+          // S buffer (N+n)&1 held S and P of tile N+n-2, read by the softmax
+          // warps before they signalled its P and by O += P V of that tile,
+          // which this thread issued earlier (in-order tcgen05.mma).
+          const int Nn = N + n;
+          const uint32_t s_col = 256 + 128 * (Nn & 1);
+          const uint32_t seq0 = seq_base + unit_k(n) * HC;
+          const int slot0 = seq0 % kSlots;
+          for (int c = 0; c < HC && ok; ++c) {
+            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t qa = sdesc_add(dq0, c * kChunkBytes);
+            const uint64_t kb = sdesc_add(dk0, (slot0 + c) * kChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + s_col, sdesc_add(qa, kk * 32), sdesc_add(kb, kk * 32), id_s,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bars.empty(slot0 + c));
+          }
+          if (!ok) break;
+          mma_commit(bars.s_full(Nn & 1));
+          if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
+        }
+        if (ok) ok = issue_pv(n_tiles - 1);
+        seq_base += 2u * n_tiles * HC;
+        N += n_tiles;
+      }
+      if (!ok) {
+        mma_commit(bars.teardown());
+        mbar_wait_teardown(bars.teardown(), 0, a.wait_limit_ns);
+      }
+    }
+  } else {
+    // --------------------------------------------------- softmax, epilogue
+    const int r = tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    int N = 0;
+    for (int k = 0; ok; ++k) {
+      const int b = k & 1;
+      if (!warp_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
+      volatile int* info = info_all + 4 * b;
+      const int n_tiles = info[0];
+      if (n_tiles < 0) break;
+      const int qt = info[1], bk = info[2], bb = bk / a.K;
+      const int t0 = qt * Tb, g = r / Tb, t = t0 + (r - g * Tb);
+      const bool valid = t < a.T;
+      const int my_seg = (segs && valid) ? a.seg_q[(long)bb * a.T + t] : 0;
+      const uint16_t* list = sched(b);
+      const uint32_t o_col = 128u * b;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int n = 0; n < n_tiles; ++n) {
+        if (!softmax_tile<H>(a, tmem, lane_base, list[n], n, N + n, t, g, valid, my_seg, bb,
+                             bk % a.K, bars, ab, m_ref, l, o_col)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      const int last = N + n_tiles - 1;
+      const bool have = n_tiles > 0 && warp_wait(bars.pv_done(last & 1), (last >> 1) & 1, ab);
+      if (n_tiles > 0 && !have) { ok = false; break; }
+      if (have) tc_fence_after();
+      const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+      const float lse_row = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      // Q[b] is free: every product of this item has completed (pv_done of its
+      // last tile follows them all), or there were none.
+      stage_o_row<H>(sm + q_tile(b), tmem, lane_base, o_col, r, have, inv);
+      if (valid) a.lse[((long)bk * a.G + g) * a.T + t] = lse_row;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, kRows);
+      if (tid == 0) {
+        for (int c = 0; c < HC; ++c)
+          tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, t0, 0, bk);
+        bulk_commit();
+        bulk_wait_read0();
+        mbar_arrive(item_free(b));  // Q[b] (staging) and O[b] may be reused
+      }
+      N += n_tiles;
+    }
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -533,6 +917,24 @@ cudaError_t launch_fwd_h(const FwdArgs& a, cudaStream_t st) {
   }
   dim3 grid(a.n_qtiles * a.B * a.K, 1, a.n_splits);
   fa_fwd_kernel<H><<<grid, kThreads, L::alloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int H>
+cudaError_t launch_fwd_persistent_h(const FwdArgs& a, int sm_count, cudaStream_t st) {
+  using L = PFwdSmem<H>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_persistent_kernel<H>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const long items = (long)a.n_qtiles * a.B * a.K;
+  const int grid = (int)(items < sm_count ? items : sm_count);
+  fa_fwd_persistent_kernel<H><<<grid, kPThreads, L::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -591,10 +993,27 @@ cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st) {
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st, int schedule) {
+  // schedule: 0 chooses (persistent for H <= 128 without split-KV when there
+  // are more Q tiles than SMs: with one tile per CTA there is nothing to
+  // overlap), 1 one CTA per Q tile, 2 persistent where supported.
+  static int cached_dev = -1, cached_sms = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return cudaErrorInvalidValue;
+    cached_sms = n;
+    cached_dev = dev;
+  }
+  const int sms = cached_sms;
+  const long items = (long)a.n_qtiles * a.B * a.K;
+  const bool supported = a.H <= 128 && a.n_splits == 1;
+  const bool persistent = supported && (schedule == 2 || (schedule == 0 && items > sms));
   switch (a.H) {
-    case 64: return launch_fwd_h<64>(a, st);
-    case 128: return launch_fwd_h<128>(a, st);
+    case 64: return persistent ? launch_fwd_persistent_h<64>(a, sms, st) : launch_fwd_h<64>(a, st);
+    case 128: return persistent ? launch_fwd_persistent_h<128>(a, sms, st) : launch_fwd_h<128>(a, st);
     case 256: return launch_fwd_h<256>(a, st);
     default: return cudaErrorInvalidValue;
   }

@@ -63,7 +63,7 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
 };
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st, int schedule);
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
                                   cudaStream_t st);
 cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st);

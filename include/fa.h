@@ -232,6 +232,17 @@ int fa_set_wait_limit_ns(uint64_t ns);
 int fa_set_bwd_kv_rows(int rows);
 
 /*
+ * Forward grid for calls made after this one: 0 (default) chooses per call, 1
+ * launches one CTA per Q tile, 2 launches one persistent CTA per SM that walks
+ * the Q tiles, the next tile's schedule, Q copy and first products overlapping
+ * the current tile's epilogue (H <= 128 without split-KV; other calls use one
+ * CTA per Q tile).  The default takes 2 where supported and the Q tiles
+ * outnumber the SMs.  The results do not depend on the choice.  Returns
+ * FA_ERR_INVALID_ARG for any other value.
+ */
+int fa_set_fwd_schedule(int mode);
+
+/*
  * Self-test of the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier no one arrives on, with the current limit, and returns the status
  * fa_check_status() reports afterwards (FA_ERR_DEVICE_TIMEOUT when the

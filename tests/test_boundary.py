@@ -111,3 +111,10 @@ def test_bwd_kv_rows_setter(clib):
         assert binding.fa_set_bwd_kv_rows(bad) == binding.FA_ERR_INVALID_ARG
     for ok in (64, 128, 0):
         assert binding.fa_set_bwd_kv_rows(ok) == binding.FA_OK
+
+
+def test_fwd_schedule_setter(clib):
+    for bad in (-1, 3, 100):
+        assert binding.fa_set_fwd_schedule(bad) == binding.FA_ERR_INVALID_ARG
+    for ok in (1, 2, 0):
+        assert binding.fa_set_fwd_schedule(ok) == binding.FA_OK

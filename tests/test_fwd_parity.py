@@ -192,3 +192,45 @@ def test_splitkv_default_splits():
     assert 1 <= n <= 64
     assert binding.fa_fwd_splitkv_default_splits(1, 2, 8, 8192, 8192, 256) == 1
     run_split(1, 8, 8, 1, 8192, 128, None, causal=True, seed=6)
+
+
+# ------------------------------------- both forward grids (H <= 128 choices)
+
+@pytest.fixture
+def fwd_schedule(request):
+    assert binding.fa_set_fwd_schedule(request.param) == binding.FA_OK
+    yield request.param
+    binding.fa_set_fwd_schedule(0)
+
+
+def _distinct_key_ids(B, T):
+    # query ids 0..3 by 128-position block, key ids reversed: whole Q tiles see no key
+    seg_q = np.repeat(np.arange(4, dtype=np.int32), T // 4)[None].repeat(B, 0)
+    seg_kv = np.repeat(np.array([3, 2, 1, 0], dtype=np.int32), T // 4)[None].repeat(B, 0)
+    seg_q[:, : T // 8] = 7  # ids no key carries
+    return seg_q, seg_kv
+
+
+GRID_CASES = {
+    "h64_causal": dict(B=1, K=2, G=4, T=384, S=384, H=64, causal=True),
+    "h128_ragged_full": dict(B=1, K=2, G=8, T=1000, S=1000, H=128, causal=False),
+    "h128_rect_causal": dict(B=2, K=2, G=4, T=100, S=300, H=128, causal=True),
+    "h128_decode": dict(B=2, K=2, G=8, T=1, S=1000, H=128, causal=True),
+    "h128_many_items": dict(B=2, K=8, G=4, T=2048, S=2048, H=128, causal=True),
+    "h128_docs_many_items": dict(B=4, K=8, G=4, T=1024, S=1024, H=128, causal=True, segs="docs"),
+    "h128_empty_q_tiles": dict(B=2, K=4, G=4, T=512, S=512, H=128, causal=False, segs="distinct"),
+}
+
+
+@pytest.mark.parametrize("fwd_schedule", [1, 2], indirect=True)
+@pytest.mark.parametrize("name", sorted(GRID_CASES))
+def test_both_forward_grids(fwd_schedule, name):
+    c = dict(GRID_CASES[name])
+    kind = c.pop("segs", None)
+    seg_q = seg_kv = None
+    if kind == "docs":
+        seg_q = seg_kv = inputs.document_segment_ids(c["B"], c["T"], seed=5, lo=40, hi=300)
+    elif kind == "distinct":
+        seg_q, seg_kv = _distinct_key_ids(c["B"], c["T"])
+    run_case(c["B"], c["K"], c["G"], c["T"], c["S"], c["H"], causal=c["causal"], seg_q=seg_q,
+             seg_kv=seg_kv, seed=len(name))

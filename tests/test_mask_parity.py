@@ -81,3 +81,13 @@ def test_block_sparse_h128_both_kv_tile_sizes(rows):
         run_masked(2, 2, 4, 300, 300, 128, 8, causal=True, segs=True, seed=rows + 1)
     finally:
         binding.fa_set_bwd_kv_rows(0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_block_sparse_forward_both_grids(mode):
+    assert binding.fa_set_fwd_schedule(mode) == binding.FA_OK
+    try:
+        run_masked(2, 4, 4, 1024, 1024, 128, 16, causal=True, seed=mode, backward=False)
+        run_masked(1, 1, 4, 256, 384, 64, 4, causal=True, seed=mode + 2, backward=False)
+    finally:
+        binding.fa_set_fwd_schedule(0)
