@@ -128,6 +128,24 @@ __device__ __forceinline__ void store_row32(uint8_t* base, int r, int c, const u
   }
 }
 
+// [lo, hi) covering every non-empty tile of a CTA's sweep, found by all
+// threads at once (one class per thread and step, loads in parallel) so that
+// the roles' loops skip the empty prefix and suffix of the sweep without one
+// serial load per skipped tile.  Called by every thread (two __syncthreads);
+// without segment ids or a block mask the classes need no loads.
+template <typename ClassOf>
+__device__ __forceinline__ int2 nonempty_range(int first, int end, int* lo_hi, ClassOf class_of) {
+  if (threadIdx.x == 0) { lo_hi[0] = end; lo_hi[1] = first; }
+  __syncthreads();
+  int lo = end, hi = first;
+  for (int x = first + (int)threadIdx.x; x < end; x += (int)blockDim.x)
+    if (class_of(x) != TILE_EMPTY) { lo = min(lo, x); hi = max(hi, x + 1); }
+  if (lo < end) atomicMin(lo_hi, lo);
+  if (hi > first) atomicMax(lo_hi + 1, hi);
+  __syncthreads();
+  return make_int2(lo_hi[0], max(lo_hi[0], lo_hi[1]));
+}
+
 // =================================================================== dQ
 template <int H, int BN_>
 struct DqCfg {
@@ -206,6 +224,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // (the loops start at 0 and skip [0, jr.x) with one compare: a loop start
+  // read back from shared memory measured 15% slower at H = 256)
+  const int2 jr = nonempty_range(0, jt_end, reinterpret_cast<int*>(sm + C::misc_off + 8), [&](int jt) {
+    return tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
+  });
 
   if (warp == 4) {
     // K producer (and the Q / dO tiles).  K chunks are held until dQ(n) is
@@ -216,8 +239,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       uint32_t seq = 0;  // chunk sequence number
       uint32_t k_issued = 0;
       bool any = false;
-      for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+      for (int jt = 0; jt < jr.y && ok; ++jt) {
+        if (jt < jr.x || tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!any) {
           any = true;
           mbar_arrive_expect_tx(q_full(), 2 * HC * kQChunk);
@@ -247,8 +270,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     if (lane == 0) {
       bool ok = true;
       uint32_t seq = 0, v_issued = 0;
-      for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+      for (int jt = 0; jt < jr.y && ok; ++jt) {
+        if (jt < jr.x || tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = seq + c;
           const int slot = sq % VSL;
@@ -290,8 +313,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
         mma_commit(dq_done(u));
         return true;
       };
-      for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+      for (int jt = 0; jt < jr.y && ok; ++jt) {
+        if (jt < jr.x || tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!waited_q) {
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
@@ -330,8 +353,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       const uint64_t dvk = sdesc_sw128(sbase + C::v_off, 16, 1024);
       bool ok = true, waited_q = false;
       int n = 0;
-      for (int jt = 0; jt < jt_end && ok; ++jt) {
-        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+      for (int jt = 0; jt < jr.y && ok; ++jt) {
+        if (jt < jr.x || tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!waited_q) {
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
@@ -374,7 +397,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
     bool ok = true;
     int n = 0;
-    for (int jt = 0; jt < jt_end; ++jt) {
+    for (int jt = 0; jt < jr.y; ++jt) {
+      if (jt < jr.x) continue;
       const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int u = n % NBUF;
@@ -519,6 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int2 qrng = nonempty_range(qt_begin, a.n_qtiles, reinterpret_cast<int*>(sm + C::misc_off + 8),
+                                   [&](int qt) { return tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN); });
 
   if (warp == 4) {
     // Producer: K, V once; per Q tile, dO (released after dV^T) then Q
@@ -527,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       bool ok = true, any = false;
       int i = 0;
       uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
-      for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
+      for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (!any) {
           any = true;
@@ -585,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const uint64_t d_z = sdesc_sw128(sbase + z_off, kQChunk, 1024);
       bool ok = true;
       int i = 0;
-      for (int qt = qt_begin; qt < a.n_qtiles && ok; ++qt) {
+      for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
         if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
         // S(i-1) was read before P(i-1) was signalled, and A waited for dS(i-1),
@@ -629,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     constexpr int NCH = BN / 64;  // 32-column chunks per warp
     bool ok = true;
     int i = 0;
-    for (int qt = qt_begin; qt < a.n_qtiles; ++qt) {
+    for (int qt = qrng.x; qt < qrng.y; ++qt) {
       const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int g = r / Tb, t = qt * Tb + (r - g * Tb);
