@@ -291,33 +291,55 @@ def ours_arm(args, world, rank, local):
         ((1 + (2 if sq is not None else 0) + 2) if w.backward else 0)
     n_ev = 5 if w.backward else 2
 
-    def step(evs=None):
+    # device buffers of one step: inputs (q, k, v, dO, seg ids) and outputs
+    bufs0 = {"q": q, "k": k, "v": v, "dO": dO, "sq": sq, "skv": skv, "o": o, "lse": lse}
+    if w.backward:
+        bufs0.update(dq=dq, dk=dk, dv=dv)
+
+    def step(evs=None, bufs=None):
+        B_ = bufs0 if bufs is None else bufs
+        q_, k_, v_, dO_, sq_, skv_ = (B_[n] for n in ("q", "k", "v", "dO", "sq", "skv"))
+        o_, lse_ = B_["o"], B_["lse"]
         if evs is not None:
             evs[0].record(stream)
         if meta is not None:
-            binding.fa_fwd_masked(q, k, v, sq, skv, w.causal, meta, o, lse, stream)
+            binding.fa_fwd_masked(q_, k_, v_, sq_, skv_, w.causal, meta, o_, lse_, stream)
         elif n_splits > 1:
-            binding.fa_fwd_splitkv(q, k, v, sq, skv, w.causal, o, lse, n_splits, ws_split, stream)
+            binding.fa_fwd_splitkv(q_, k_, v_, sq_, skv_, w.causal, o_, lse_, n_splits, ws_split,
+                                   stream)
         else:
-            binding.fa_fwd(q, k, v, sq, skv, w.causal, o, lse, stream)
+            binding.fa_fwd(q_, k_, v_, sq_, skv_, w.causal, o_, lse_, stream)
         if evs is not None:
             evs[1].record(stream)
-        if w.backward and meta is not None:
+        if not w.backward:
+            return
+        dq_, dk_, dv_ = B_["dq"], B_["dk"], B_["dv"]
+        if meta is not None:
             # the masked backward runs its stages back to back (one call)
-            binding.fa_bwd_masked(q, k, v, o, lse, dO, sq, skv, w.causal, meta, dq, dk, dv, ws,
-                                  stream)
+            binding.fa_bwd_masked(q_, k_, v_, o_, lse_, dO_, sq_, skv_, w.causal, meta, dq_, dk_,
+                                  dv_, ws, stream)
             if evs is not None:
                 for i in (2, 3, 4):
                     evs[i].record(stream)
-        elif w.backward and evs is None:
+        elif evs is None:
             # one call: the dQ grid may overlap the tail of the dK/dV grid
-            binding.fa_bwd(q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws, stream)
-        elif w.backward:
+            binding.fa_bwd(q_, k_, v_, o_, lse_, dO_, sq_, skv_, w.causal, dq_, dk_, dv_, ws, stream)
+        else:
             # stage by stage with events between them: per-kernel durations
             for st in range(3):
-                binding.fa_bwd_stage(st, q, k, v, o, lse, dO, sq, skv, w.causal, dq, dk, dv, ws,
-                                     stream)
+                binding.fa_bwd_stage(st, q_, k_, v_, o_, lse_, dO_, sq_, skv_, w.causal, dq_, dk_,
+                                     dv_, ws, stream)
                 evs[2 + st].record(stream)
+
+    # Inputs and outputs smaller than L2: write a buffer of twice L2 between
+    # timed steps (outside their events) so that no step starts L2-warm.
+    in_bytes = sum(t.numel() * t.element_size() for t in bufs0.values() if t is not None)
+    small = in_bytes <= L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
+
+    def flush():
+        if flush_buf is not None:
+            flush_buf.fill_(1)
 
     for _ in range(args.warmup):
         step()
@@ -330,23 +352,36 @@ def ours_arm(args, world, rank, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step()
-    t_end.record(stream)
+    if small:
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            step_ev[i][0].record(stream)
+            step()
+            step_ev[i][1].record(stream)
+    else:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step()
+        t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     status = binding.fa_check_status(stream)
     assert status == binding.FA_OK, binding.status_string(status)
-    ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dev)
+    if small:
+        ms = reduce_max(sum(a_.elapsed_time(b_) for a_, b_ in step_ev) / args.steps, dev)
+    else:
+        ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dev)
 
     # per-kernel device time: a second loop, stage by stage with CUDA events
     # between the launches (which also keeps dQ from overlapping dK/dV there)
     n_k = max(3, min(args.steps, 20))
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_k)]
     for i in range(n_k):
+        flush()
         step(events[i])
     torch.cuda.synchronize()
     per = {}
@@ -415,9 +450,67 @@ def ours_arm(args, world, rank, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_serial_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dev)
 
-    in_bytes = sum(t.numel() * t.element_size() for t in dev_in + outs)
+    # Pipelined: two device buffer sets; step i's inputs are copied in on one
+    # stream and step i-1's results copied out on another while step i-1 / i
+    # compute, as a training loop with prefetch would.  Every step still moves
+    # its inputs from pinned host memory and its results back.
+    in_names = [n for n in ("q", "k", "v", "dO", "sq", "skv") if bufs0[n] is not None]
+    out_names = ["o", "lse"] + (["dq", "dk", "dv"] if w.backward else [])
+    bufs1 = {n: (torch.empty_like(t) if t is not None else None) for n, t in bufs0.items()}
+    sets = [bufs0, bufs1]
+    host_src = dict(zip(["q", "k", "v"] + (["dO"] if w.backward else []), host_in))
+    if seg_host:
+        host_src.update(sq=seg_host[0], skv=seg_host[1])
+    host_dst = [dict(zip(out_names, host_out)),
+                {n: torch.empty(bufs0[n].shape, dtype=bufs0[n].dtype, pin_memory=True)
+                 for n in out_names}]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_pipelined(n_steps):
+        ev = [{k_: torch.cuda.Event() for k_ in ("h2d", "comp", "d2h")} for _ in range(n_steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n_steps):
+            b_ = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev[i - 2]["comp"])  # inputs of set b_ were read
+                for n in in_names:
+                    sets[b_][n].copy_(host_src[n], non_blocking=True)
+                ev[i]["h2d"].record(s_in)
+            stream.wait_event(ev[i]["h2d"])
+            if i >= 2:
+                stream.wait_event(ev[i - 2]["d2h"])  # outputs of set b_ were read back
+            step(bufs=sets[b_])
+            ev[i]["comp"].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev[i]["comp"])
+                for n in out_names:
+                    host_dst[b_][n].copy_(sets[b_][n], non_blocking=True)
+                ev[i]["d2h"].record(s_out)
+        stream.wait_event(ev[n_steps - 1]["d2h"])
+        stream.wait_event(ev[n_steps - 1]["h2d"])
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / n_steps
+
+    e2e_pipelined(2)
+    e2e_ms = reduce_max(e2e_pipelined(e2e_steps), dev)
+    # both are end to end (every step's inputs in, results out); report the faster
+    if e2e_ms <= e2e_serial_ms:
+        e2e_best, e2e_mode = e2e_ms, ("pipelined: H2D of step i and D2H of step i-1 on two copy "
+                                      "streams overlap the kernels (two device buffer sets)")
+    else:
+        e2e_best, e2e_mode = e2e_serial_ms, "serial: H2D, kernels, D2H in order on one stream"
+    torch.cuda.synchronize()
+    status = binding.fa_check_status(stream)
+    assert status == binding.FA_OK, binding.status_string(status)
+
     line = {
         "metric": METRIC,
         "value": round(world * step_flop / (ms * 1e-3) / 1e12, 2),
@@ -435,12 +528,16 @@ def ours_arm(args, world, rank, local):
                    "window": w.window or None,
                    "pct_of_peak": round(100 * step_flop / (ms * 1e-3) / 1e12 / peak, 2),
                    "l2": f"inputs+outputs {in_bytes / 2**20:.0f} MiB vs L2 {L2_BYTES / 2**20:.0f} MiB"
-                         + (" (larger: no flush)" if in_bytes > L2_BYTES else " (smaller than L2)"),
+                         + (" (larger: no flush)" if not small else
+                            f" (smaller: {2 * L2_BYTES / 2**20:.0f} MiB written between timed steps, "
+                            "each step timed by its own events)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
-        "e2e": {"value": round(world * step_flop / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(world * step_flop / (e2e_best * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_best, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "mode": e2e_mode,
+                "pipelined_ms_per_step": round(e2e_ms, 4),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
