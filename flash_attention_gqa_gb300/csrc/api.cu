@@ -230,8 +230,11 @@ int fa_fwd_splitkv_default_splits(int B, int K, int G, int T, int S, int H) {
   const int sms = fa_device_sm_count();
   const int kv_tiles = (S + fa::kKvRows - 1) / fa::kKvRows;
   // Splitting costs partial writes and a merge: only worth it when the Q
-  // tiles alone leave SMs idle.
-  long n = (sms > 0 && ctas < sms) ? (2L * sms + ctas - 1) / ctas : 1;
+  // tiles alone leave SMs idle.  Then as many splits as fit in one wave: a
+  // sweep of 1-64 splits on decode shapes (8-64 kv heads, S = 8K-32K, H = 128
+  // and 256) put the fastest count at or within 5% of floor(SMs / CTAs); a
+  // second, partial wave costs more than it adds.
+  long n = (sms > 0 && ctas < sms) ? sms / ctas : 1;
   n = n < 1 ? 1 : n;
   n = n > kv_tiles ? kv_tiles : n;
   return (int)(n > 64 ? 64 : n);

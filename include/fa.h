@@ -87,9 +87,9 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v,
 /* Workspace bytes of fa_fwd_splitkv (0 for unsupported sizes or n_splits). */
 size_t fa_fwd_splitkv_workspace_size(int B, int K, int G, int T, int S, int H, int n_splits);
 
-/* A split count that gives about two CTAs per SM of the current device when
-   the Q tiles alone number fewer CTAs than SMs (1 otherwise); at most 64 and
-   at most the number of KV tiles. */
+/* A split count that fills one wave of the current device, floor(SMs / CTAs)
+   where the Q tiles alone number fewer CTAs than SMs (1 otherwise); at most 64
+   and at most the number of KV tiles. */
 int fa_fwd_splitkv_default_splits(int B, int K, int G, int T, int S, int H);
 
 /*
