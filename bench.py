@@ -41,10 +41,10 @@ L2_BYTES = 129 * 2**20
 # DRAM traffic per launch of the roofline kernel from one ncu capture, keyed
 # by kernel name; valid only while the kernel source hashes to `src_sha`.
 NCU_TRAFFIC = {
-    # one --metrics capture of the causal H=256, T=S=8192 step: mean of 11 launches
-    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 230800000, "src_sha": "9f3e55838991a9eb"},
-    "fa_bwd_dq_kernel": {"bytes_per_launch": 191700000, "src_sha": "9f3e55838991a9eb"},
-    "fa_fwd_kernel": {"bytes_per_launch": 111500000, "src_sha": "206a8489137e198d"},
+    # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
+    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 274370000, "src_sha": "a1b019ab124a584e"},
+    "fa_bwd_dq_kernel": {"bytes_per_launch": 191350000, "src_sha": "a1b019ab124a584e"},
+    "fa_fwd_kernel": {"bytes_per_launch": 111020000, "src_sha": "ff8487c7a750f28e"},
 }
 
 
