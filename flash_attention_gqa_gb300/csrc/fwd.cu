@@ -537,10 +537,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 // buffered (b = local item index & 1), so a scheduler warp classifies the KV
 // tiles of item k+1 and starts its Q copy while item k runs, and the MMA warp
 // computes the first S tiles of item k+1 while the softmax warps finish item
-// k's epilogue.  Roles (224 threads): warps 0-3 softmax and epilogue, warp 4
-// K/V producer, warp 5 MMA issuer and TMEM owner, warp 6 scheduler.  Tensor
-// memory: O[b] at columns [128 b, 128 b + H), S buffers at 256 and 384.
-constexpr int kPThreads = 224;
+// k's epilogue.  Roles (256 threads): warps 0-3 softmax and epilogue, warp 4
+// K/V producer, warp 5 S = Q K^T issuer and TMEM owner, warp 6 scheduler,
+// warp 7 O += P V issuer.  One thread issuing both products is the limit at
+// H <= 128 (a trace: ~87 cycles per S product and ~123 per P V product against
+// 64 on the tensor pipe), so each product type has its own issuing warp.
+// Tensor memory: O[b] at columns [128 b, 128 b + H), S buffers at 256 and 384.
+constexpr int kPThreads = 256;
 
 template <int H>
 struct PFwdSmem {
@@ -550,8 +553,8 @@ struct PFwdSmem {
   static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[2][kMaxKvTiles]
   static constexpr uint32_t bar_off = sched_off + 2 * kMaxKvTiles * 2;
   // q_full[2], sched_full[2], item_free[2], then the Bars block (full, empty,
-  // s_full, p_full, pv_done, teardown)
-  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7;
+  // s_full, p_full, pv_done, teardown), then the O += P V issuer's teardown
+  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7 + 1;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, item info[2][4]
   static constexpr uint32_t bytes = misc_off + 64;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -571,6 +574,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
   auto sched_full = [&](int b) { return pb + 8 * (2 + b); };
   auto item_free = [&](int b) { return pb + 8 * (4 + b); };
   Bars bars{pb + 8 * 6};
+  const uint32_t teardown_pv = pb + 8 * (6 + 1 + 2 * kSlots + 7);
   auto sched = [&](int b) { return reinterpret_cast<uint16_t*>(sm + L::sched_off) + b * kMaxKvTiles; };
   auto q_tile = [&](int b) { return L::q_off + (uint32_t)b * HC * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
@@ -591,9 +595,9 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
     for (int b = 0; b < 2; ++b) {
       mbar_init(q_full(b), 1);
       mbar_init(sched_full(b), 1);
-      // producer done with the schedule, MMA warp has read the tile count,
-      // epilogue stored: the item's buffers may be refilled
-      mbar_init(item_free(b), 3);
+      // producer done with the schedule, both MMA warps have read the tile
+      // count, epilogue stored: the item's buffers may be refilled
+      mbar_init(item_free(b), 4);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(bars.full(s), 1);
@@ -605,6 +609,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
+    mbar_init(teardown_pv, 1);
     fence_barrier_init();
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
@@ -752,12 +757,10 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       }
     }
   } else if (warp == 5) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
-      constexpr uint32_t id_o = idesc_bf16(128, H, false, true);     // O += P V (N = H)
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       const uint64_t dk0 = sdesc_sw128(sbase + L::ring_off, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(sbase + L::ring_off, kChunkBytes, 1024);
       bool ok = true;
       uint32_t seq_base = 0;  // ring chunks of earlier items
       int N = 0;              // tiles of earlier items (S / P buffer and parity counter)
@@ -766,36 +769,16 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
         if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
         const int n_tiles = info_all[4 * b];
         if (n_tiles < 0) break;
-        // Nothing else of the item's shared state is read here (O[b] and Q[b]
-        // are released by the epilogue, which waits for this warp's products).
+        // Nothing else of the item's shared state is read here (Q[b] is
+        // released by the epilogue, which waits for every product of the item).
         mbar_arrive(item_free(b));
         if (n_tiles == 0) continue;
         if (!mbar_wait(q_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
         const uint64_t dq0 = sdesc_sw128(sbase + q_tile(b), 16, 1024);
-        const uint32_t o_col = 128u * b;
-        auto issue_pv = [&](int n) -> bool {
-          const int Nn = N + n;
-          if (!mbar_wait(bars.p_full(Nn & 1), (Nn >> 1) & 1, ab)) return false;
-          const uint32_t seq0 = seq_base + unit_v(n, n_tiles) * HC;
-          const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
-          for (int c = 0; c < HC; ++c)
-            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) return false;
-          tc_fence_after();
-          const uint32_t p_col = 256 + 128 * (Nn & 1);
-          const uint64_t bv = sdesc_add(dv0, slot0 * kChunkBytes);
-#pragma unroll
-          for (int kk = 0; kk < kKvRows / 16; ++kk)
-            mma_ts(tmem + o_col, tmem + p_col + kk * 8, sdesc_add(bv, kk * 2048), id_o,
-                   (n > 0 || kk > 0) ? 1u : 0u);
-          for (int c = 0; c < HC; ++c) mma_commit(bars.empty(slot0 + c));
-          mma_commit(bars.pv_done(Nn & 1));
-          return true;
-        };
         for (int n = 0; n < n_tiles && ok; ++n) {
-          // S buffer (N+n)&1 held S and P of tile N+n-2, read by the softmax
-          // warps before they signalled its P and by O += P V of that tile,
-          // which this thread issued earlier (in-order tcgen05.mma).
           const int Nn = N + n;
+          // S buffer Nn&1 holds P of tile Nn-2 until O += P V of that tile is done.
+          if (Nn >= 2 && !mbar_wait(bars.pv_done(Nn & 1), ((Nn - 2) >> 1) & 1, ab)) { ok = false; break; }
           const uint32_t s_col = 256 + 128 * (Nn & 1);
           const uint32_t seq0 = seq_base + unit_k(n) * HC;
           const int slot0 = seq0 % kSlots;
@@ -812,15 +795,54 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           }
           if (!ok) break;
           mma_commit(bars.s_full(Nn & 1));
-          if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
         }
-        if (ok) ok = issue_pv(n_tiles - 1);
         seq_base += 2u * n_tiles * HC;
         N += n_tiles;
       }
       if (!ok) {
         mma_commit(bars.teardown());
         mbar_wait_teardown(bars.teardown(), 0, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------ O += P V issuer
+    if (lane == 0) {
+      constexpr uint32_t id_o = idesc_bf16(128, H, false, true);  // N = H, V MN-major
+      const uint64_t dv0 = sdesc_sw128(sbase + L::ring_off, kChunkBytes, 1024);
+      bool ok = true;
+      uint32_t seq_base = 0;
+      int N = 0;
+      for (int k = 0; ok; ++k) {
+        const int b = k & 1;
+        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
+        const int n_tiles = info_all[4 * b];
+        if (n_tiles < 0) break;
+        mbar_arrive(item_free(b));
+        const uint32_t o_col = 128u * b;  // free: sched_full(b) follows item k-2's epilogue
+        for (int n = 0; n < n_tiles && ok; ++n) {
+          const int Nn = N + n;
+          if (!mbar_wait(bars.p_full(Nn & 1), (Nn >> 1) & 1, ab)) { ok = false; break; }
+          const uint32_t seq0 = seq_base + unit_v(n, n_tiles) * HC;
+          const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
+          for (int c = 0; c < HC && ok; ++c)
+            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t p_col = 256 + 128 * (Nn & 1);
+          const uint64_t bv = sdesc_add(dv0, slot0 * kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKvRows / 16; ++kk)
+            mma_ts(tmem + o_col, tmem + p_col + kk * 8, sdesc_add(bv, kk * 2048), id_o,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < HC; ++c) mma_commit(bars.empty(slot0 + c));
+          mma_commit(bars.pv_done(Nn & 1));
+        }
+        seq_base += 2u * n_tiles * HC;
+        N += n_tiles;
+      }
+      if (!ok) {
+        mma_commit(teardown_pv);
+        mbar_wait_teardown(teardown_pv, 0, a.wait_limit_ns);
       }
     }
   } else {
