@@ -146,6 +146,15 @@ __device__ __forceinline__ int2 nonempty_range(int first, int end, int* lo_hi, C
   return make_int2(lo_hi[0], max(lo_hi[0], lo_hi[1]));
 }
 
+// Wait (whole warp) for the release barrier of every head-dim half.
+template <int HH, typename F>
+__device__ __forceinline__ bool wait_halves(F bar, uint32_t parity, const Abort& ab) {
+#pragma unroll
+  for (int h = 0; h < HH; ++h)
+    if (!warp_wait(bar(h), parity, ab)) return false;
+  return true;
+}
+
 // =================================================================== dQ
 template <int H, int BN_>
 struct DqCfg {
@@ -466,8 +475,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
 }
 
 // ================================================================ dK/dV
+// One Q stage (H = 256: a second 64 KB Q tile does not fit next to K, V, dO, P
+// and dS).  S(i+1) follows dK^T(i), which reads the only Q buffer.
 template <int H, int BN_>
-struct DkvCfg {
+struct Dkv1Cfg {
   static constexpr int BN = BN_;              // keys per CTA
   static constexpr int HC = H / 64;
   static constexpr int HH = H / 128;          // 128-lane halves of the head dim
@@ -491,8 +502,8 @@ struct DkvCfg {
 };
 
 template <int H, int BN_>
-__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
-  using C = DkvCfg<H, BN_>;
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_constant__ BwdArgs a) {
+  using C = Dkv1Cfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -746,6 +757,358 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
 }
 
+// ======================================================== dK/dV, two Q stages
+// H = 128: the next Q tile has its own stage, so S(i+1) is issued as soon as the
+// softmax side has read S(i) and the next tile's exponentials overlap this
+// tile's dK^T / dV^T products.
+template <int H, int BN_>
+struct DkvCfg {
+  static constexpr int BN = BN_;              // keys per CTA
+  static constexpr int HC = H / 64;
+  static constexpr int HH = H / 128;          // 128-lane halves of the head dim
+  static constexpr int PC = BN / 64;          // 64-key chunks of P / dS
+  // Q stages.  With H = 128 a second Q tile fits: S of the next Q tile is then
+  // computed while the softmax side and dK^T / dV^T still work on this one.
+  static constexpr int QB = 2;
+  static_assert(H == 128, "two Q stages fit in shared memory at H = 128");
+  static constexpr uint32_t KV_CHUNK = BN * 128;
+  static constexpr uint32_t k_off = 0;
+  static constexpr uint32_t v_off = HC * KV_CHUNK;
+  static constexpr uint32_t q_off = 2 * HC * KV_CHUNK;  // QB stages of HC chunks
+  static constexpr uint32_t do_off = q_off + QB * HC * kQChunk;
+  static constexpr uint32_t p_off = do_off + HC * kQChunk;
+  static constexpr uint32_t ds_off = p_off + PC * kQChunk;
+  static constexpr uint32_t bar_off = ds_off + PC * kQChunk;
+  // kv_full, s_full, dp_full, p_full, ds_full, teardown[2], q_full[QB][HC],
+  // do_full[HC], q_empty[QB][HH], do_empty[HH]
+  static constexpr int n_bars = 7 + QB * HC + HC + QB * HH + HH;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;
+  static constexpr uint32_t alloc = misc_off + 64 + 1024;
+  static_assert(alloc <= 232448, "shared memory per CTA");
+  static constexpr uint32_t dv_col = 0;
+  static constexpr uint32_t dk_col = HH * BN;
+  static constexpr uint32_t s_col = 2 * HH * BN;
+  static constexpr uint32_t dp_col = 2 * HH * BN + BN;
+};
+
+template <int H, int BN_>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  using C = DkvCfg<H, BN_>;
+  constexpr int HC = C::HC, HH = C::HH, BN = C::BN, QB = C::QB;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + C::bar_off;
+  const uint32_t kv_full = bar0, s_full = bar0 + 8, dp_full = bar0 + 16;
+  const uint32_t p_full = bar0 + 24, ds_full = bar0 + 32;
+  auto teardown = [&](int i) { return bar0 + 8 * (5 + i); };
+  // Tile i (i-th non-empty Q tile) uses Q stage i % QB, the (i / QB)-th use of it.
+  auto q_full = [&](int qb, int c) { return bar0 + 8 * (7 + qb * HC + c); };
+  auto do_full = [&](int c) { return bar0 + 8 * (7 + QB * HC + c); };
+  // Q (dO) 128-dim half h is released once dK^T (dV^T) of that half is done.
+  auto q_empty = [&](int qb, int h) { return bar0 + 8 * (7 + QB * HC + HC + qb * HH + h); };
+  auto do_empty = [&](int h) { return bar0 + 8 * (7 + QB * HC + HC + QB * HH + h); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::misc_off + 4);
+  const Abort ab{abort_flag, a.wait_limit_ns, a.err};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Tb = kRows / a.G;
+  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head first.
+  const int BKn = a.B * a.K;
+  const int jt = (int)(blockIdx.x / BKn);
+  const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
+  // The dQ kernel reads nothing this kernel writes: let it be scheduled on SMs
+  // this grid frees in its tail (it is launched with programmatic serialization).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int s0 = jt * BN;
+  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* kr = qr + (long)a.B * a.n_qtiles;
+  const int qt_begin = causal_first_qtile(a, s0, Tb);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(kv_full, 1);
+    for (int h = 0; h < HH; ++h) {
+      mbar_init(do_empty(h), 1);
+      for (int qb = 0; qb < QB; ++qb) mbar_init(q_empty(qb, h), 1);
+    }
+    mbar_init(s_full, 1);           // S done (issuer A's commit)
+    mbar_init(dp_full, 1);          // dP done (issuer B's commit)
+    mbar_init(p_full, 2 * kRows);   // P written (softmax side)
+    mbar_init(ds_full, 2 * kRows);  // dS written (softmax side)
+    mbar_init(teardown(0), 1);
+    mbar_init(teardown(1), 1);
+    for (int c = 0; c < HC; ++c) {
+      mbar_init(do_full(c), 1);
+      for (int qb = 0; qb < QB; ++qb) mbar_init(q_full(qb, c), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int2 qrng = nonempty_range(qt_begin, a.n_qtiles, reinterpret_cast<int*>(sm + C::misc_off + 8),
+                                   [&](int qt) { return tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN); });
+
+  if (warp == 4) {
+    // Producer: K, V once; per Q tile, dO (released after dV^T) then Q
+    // (released after dK^T), one barrier per 64-dim chunk.
+    if (lane == 0) {
+      bool ok = true, any = false;
+      int i = 0;
+      uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
+      for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (!any) {
+          any = true;
+          mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
+          for (int c = 0; c < HC; ++c) {
+            tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
+            tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
+          }
+        }
+        issued = 0;
+        const int qb = i % QB;
+        auto load_q = [&](int h) -> bool {
+          // stage qb was last read by dK^T of tile i - QB
+          if (i >= QB && !mbar_wait(q_empty(qb, h), ((i / QB) - 1) & 1, ab)) return false;
+          for (int c = 2 * h; c < 2 * h + 2; ++c) {
+            mbar_arrive_expect_tx(q_full(qb, c), kQChunk);
+            tma_load_4d(sbase + C::q_off + (qb * HC + c) * kQChunk, &a.tm_q, q_full(qb, c), c * 64,
+                        qt * Tb, 0, bk);
+            issued |= 1u << c;
+          }
+          return true;
+        };
+        auto load_do = [&](int h) -> bool {
+          if (i > 0 && !mbar_wait(do_empty(h), (i - 1) & 1, ab)) return false;
+          for (int c = 2 * h; c < 2 * h + 2; ++c) {
+            mbar_arrive_expect_tx(do_full(c), kQChunk);
+            tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, do_full(c), c * 64, qt * Tb, 0, bk);
+            issued |= 1u << (HC + c);
+          }
+          return true;
+        };
+        // Q first: its stage frees with dK^T of tile i - 2, long before dO's.
+        for (int h = 0; h < HH && ok; ++h) ok = load_q(h);
+        for (int h = 0; h < HH && ok; ++h) ok = load_do(h);
+        if (!ok) break;
+        ++i;
+      }
+      if (!ok) {
+        // Let the copies of the tile being loaded land before the CTA exits.
+        const int last = i;  // the tile being loaded when the producer gave up
+        for (int c = 0; c < HC; ++c) {
+          if (issued & (1u << c))
+            mbar_wait_teardown(q_full(last % QB, c), (last / QB) & 1, a.wait_limit_ns);
+          if (issued & (1u << (HC + c))) mbar_wait_teardown(do_full(c), last & 1, a.wait_limit_ns);
+        }
+      }
+    }
+  } else if (warp == 5 || warp == 6) {
+    // Two MMA issuers: A (warp 5) issues S = Q K^T and dK^T += Q^T dS (the Q
+    // operand), B (warp 6) issues dP = dO V^T and dV^T += dO^T P (the dO operand).
+    // P needs only S, so dV^T(i) starts while the softmax side still computes
+    // dS(i) = P (dP - D); dK^T(i) follows once dS(i) is written.  A issues
+    // S(i+1) (the other Q stage) as soon as the softmax side has read S(i),
+    // before dK^T(i), so the next tile's exponentials overlap this tile's products.
+    if (lane == 0) {
+      const bool is_a = warp == 5;
+      constexpr uint32_t id_s = idesc_bf16(128, BN, false, false);  // S, dP: [128 q x BN]
+      constexpr uint32_t id_t = idesc_bf16(128, BN, true, true);    // dV^T, dK^T: [128 h x BN]
+      const uint64_t d_k = sdesc_sw128(sbase + C::k_off, 16, 1024);
+      const uint64_t d_v = sdesc_sw128(sbase + C::v_off, 16, 1024);
+      const uint64_t d_do = sdesc_sw128(sbase + C::do_off, 16, 1024);
+      const uint64_t d_z = sdesc_sw128(sbase + (is_a ? C::ds_off : C::p_off), kQChunk, 1024);
+      const uint32_t acc_col = is_a ? C::dk_col : C::dv_col;         // dK^T or dV^T
+      bool ok = true;
+      // S(n) = Q(n) K^T from Q stage n % QB.
+      auto issue_s = [&](int n) -> bool {
+        const int qb = n % QB;
+        const uint64_t d_q = sdesc_sw128(sbase + C::q_off + qb * HC * kQChunk, 16, 1024);
+        for (int c = 0; c < HC; ++c) {
+          if (!mbar_wait(q_full(qb, c), (n / QB) & 1, ab)) return false;
+          tc_fence_after();
+          const uint64_t xa = sdesc_add(d_q, c * kQChunk), yb = sdesc_add(d_k, c * C::KV_CHUNK);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::s_col, sdesc_add(xa, kk * 32), sdesc_add(yb, kk * 32), id_s,
+                   (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        return true;
+      };
+      // dK^T (dV^T) += X^T Z over the 128 packed query rows: X = Q of tile n's
+      // stage (or dO), Z = dS (or P); releases X half by half.
+      auto issue_acc = [&](int n, uint32_t x_off) {
+        const uint64_t d_xT = sdesc_sw128(sbase + x_off, kQChunk, 1024);  // X^T, MN-major
+        for (int h = 0; h < HH; ++h) {
+          const uint64_t xA = sdesc_add(d_xT, 2 * h * kQChunk);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + acc_col + h * BN, sdesc_add(xA, kk * 2048), sdesc_add(d_z, kk * 2048), id_t,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(is_a ? q_empty(n % QB, h) : do_empty(h));
+        }
+      };
+      // next non-empty Q tile after qt (qrng.y if none)
+      auto next_tile = [&](int qt) {
+        for (++qt; qt < qrng.y; ++qt)
+          if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) != TILE_EMPTY) break;
+        return qt;
+      };
+      int i = 0;
+      for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
+        if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
+        if (i == 0 && !mbar_wait(kv_full, 0, ab)) { ok = false; break; }
+        if (is_a) {
+          if (i == 0 && !issue_s(0)) { ok = false; break; }
+          const bool more = next_tile(qt) < qrng.y;
+          // S(i+1) overwrites S(i) in TMEM: after the softmax side read it (p_full).
+          if (more && (!mbar_wait(p_full, i & 1, ab) || !issue_s(i + 1))) { ok = false; break; }
+          if (!mbar_wait(ds_full, i & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          issue_acc(i, C::q_off + (i % QB) * HC * kQChunk);
+        } else {
+          // dP(i-1) is read by the softmax side until it signals dS(i-1).
+          if (i > 0 && !mbar_wait(ds_full, (i - 1) & 1, ab)) { ok = false; break; }
+          for (int c = 0; c < HC && ok; ++c) {
+            if (!mbar_wait(do_full(c), i & 1, ab)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t xa = sdesc_add(d_do, c * kQChunk);
+            const uint64_t yb = sdesc_add(d_v, c * C::KV_CHUNK);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + C::dp_col, sdesc_add(xa, kk * 32), sdesc_add(yb, kk * 32), id_s,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          mma_commit(dp_full);
+          if (!mbar_wait(p_full, i & 1, ab)) { ok = false; break; }
+          tc_fence_after();
+          issue_acc(i, C::do_off);
+        }
+        ++i;
+      }
+      if (!ok) {
+        mma_commit(teardown(is_a ? 0 : 1));
+        mbar_wait_teardown(teardown(is_a ? 0 : 1), 0, a.wait_limit_ns);
+      }
+    }
+  } else {
+    // Softmax side: the row reads TMEM lane quadrant warp % 4; the two warps of
+    // a quadrant split the key columns (no row reduction is needed: lse and D
+    // are precomputed).
+    const int quad = warp & 3, half = warp >= 7 ? 1 : 0;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    constexpr int NCH = BN / 64;  // 32-column chunks per warp
+    bool ok = true;
+    int i = 0;
+    for (int qt = qrng.x; qt < qrng.y; ++qt) {
+      const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
+      if (cls == TILE_EMPTY) continue;
+      const int g = r / Tb, t = qt * Tb + (r - g * Tb);
+      const bool valid = t < a.T;  // rows past T (ragged last tile) are inert
+      const long row = ((long)bk * a.G + g) * a.T + t;
+      const float lse = valid ? a.lse[row] : -INFINITY;
+      const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+      const float Dr = valid ? a.delta[row] : 0.f;
+      const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
+      // Phase 1: P = exp(S - lse) once S(i) is done, computed into registers
+      // first; the P buffer is then overwritten once its reader dV^T(i-1)
+      // (issuer B's) is done.
+      if (!warp_wait(s_full, i & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pp[NCH][16];  // this warp's P (bf16 pairs), kept for phase 2
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
+        tmem_wait_ld();
+        float* sf = reinterpret_cast<float*>(sv);
+        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pp[cc][k] = pack_bf16x2(fast_exp2(fmaf(sf[2 * k], kLog2e, -lse2)),
+                                  fast_exp2(fmaf(sf[2 * k + 1], kLog2e, -lse2)));
+      }
+      if (i > 0 && !wait_halves<HH>(do_empty, (i - 1) & 1, ab)) { ok = false; break; }
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) store_row32(sm + C::p_off, r, half * NCH + cc, pp[cc]);
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor cores
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // Phase 2: dS = P (dP - D) once dP(i) is done (masked entries have P = 0).
+      // The dS buffer's reader is dK^T(i-1), which A issued after S(i), so its
+      // release barrier is waited for.
+      if (!warp_wait(dp_full, i & 1, ab)) { ok = false; break; }
+      if (i > 0) {
+        const int pq = (i - 1) % QB;
+        if (!wait_halves<HH>([&](int h) { return q_empty(pq, h); }, ((i - 1) / QB) & 1, ab)) { ok = false; break; }
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;
+        uint32_t pv[32], dd[16];
+        tmem_ld32(tmem + lane_base + C::dp_col + c * 32, pv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 pk = unpack_bf16x2(pp[cc][k]);
+          dd[k] = pack_bf16x2(pk.x * (__uint_as_float(pv[2 * k]) - Dr),
+                              pk.y * (__uint_as_float(pv[2 * k + 1]) - Dr));
+        }
+        store_row32(sm + C::ds_off, r, c, dd);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      ++i;
+    }
+    // Epilogue: lanes carry the head dim, columns the keys.
+    const int lq = (i - 1) % QB;  // Q stage of the last tile
+    const bool have = i > 0 && ok &&
+                      wait_halves<HH>([&](int h) { return q_empty(lq, h); }, ((i - 1) / QB) & 1, ab) &&
+                      wait_halves<HH>(do_empty, (i - 1) & 1, ab);
+    if (have) tc_fence_after();
+    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
+    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
+#pragma unroll 1
+    for (int h = 0; h < HH; ++h) {
+      const int hd = h * 128 + r;
+#pragma unroll 1
+      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
+        uint32_t vv[32], kv[32];
+        if (have) {
+          tmem_ld32(tmem + lane_base + C::dv_col + h * BN + c, vv);
+          tmem_ld32(tmem + lane_base + C::dk_col + h * BN + c, kv);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
+            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
+            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
 // D[row] = sum_h dO[row, h] * o[row, h] in fp32.  H / 8 lanes share a row
 // (one 16-byte load of o and of dO each); a warp covers 32 / (H / 8) rows per
 // step and takes kPreSteps steps with all loads issued before any is used, so
@@ -849,6 +1212,15 @@ cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int H, int BN>
+cudaError_t launch_dkdv1_h(const BwdArgs& a, cudaStream_t st) {
+  static int configured = -1;
+  cudaError_t e = set_smem(fa_bwd_dkdv1_kernel<H, BN>, Dkv1Cfg<H, BN>::alloc, &configured);
+  if (e != cudaSuccess) return e;
+  fa_bwd_dkdv1_kernel<H, BN><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, Dkv1Cfg<H, BN>::alloc, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
@@ -894,7 +1266,7 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
   if (a.H == 128 && a.kv_rows == 128) return launch_dkdv_h<128, 128>(a, st);
   if (a.H == 128 && a.kv_rows == 64) return launch_dkdv_h<128, 64>(a, st);
-  if (a.H == 256 && a.kv_rows == 64) return launch_dkdv_h<256, 64>(a, st);
+  if (a.H == 256 && a.kv_rows == 64) return launch_dkdv1_h<256, 64>(a, st);
   return cudaErrorNotSupported;
 }
 
