@@ -160,11 +160,18 @@ template <int H, int BN_>
 struct DqCfg {
   static constexpr int BN = BN_;                       // keys per KV tile
   static constexpr int HC = H / 64;
-  static constexpr int NBUF = (H + 4 * BN <= 512) ? 2 : 1;  // S/dP TMEM buffers
+  // TMEM buffers for S (dS overwrites it) and dP next to the H columns of dQ.
+  // Two S buffers let S(n+1) run during the softmax of tile n; with H = 128,
+  // BN = 128 only one dP buffer fits besides them (dQ 128 + S 2x128 + dP 128).
+  static constexpr int NBS = (H + 3 * BN <= 512) ? 2 : 1;
+  static constexpr int NBP = (H + NBS * BN + 2 * BN <= 512) ? 2 : 1;
+  static_assert(H + (NBS + NBP) * BN <= 512, "tensor memory");
   static constexpr uint32_t KV_CHUNK = BN * 128;       // [BN rows x 64 dims]
-  // K chunks live from S(n) to dQ(n) (two tiles in flight); V chunks from
-  // dP(n) only.  Separate rings keep the two lifetimes from blocking each other.
-  static constexpr int KSL = 2 * HC;
+  // K chunks live from S(n) to dQ(n), which trails S by NBS - 1 tiles; V chunks
+  // from dP(n) only.  Separate rings keep the two lifetimes from blocking each
+  // other.  H = 128 has room for a third K tile, so K(n+1) need not wait for
+  // dQ(n-1).
+  static constexpr int KSL = H == 256 ? 2 * HC : 3 * HC;
   static constexpr int VSL = H == 256 ? HC : 2 * HC;
   static constexpr uint32_t q_off = 0;
   static constexpr uint32_t do_off = HC * kQChunk;
@@ -175,14 +182,16 @@ struct DqCfg {
   static constexpr int n_bars = 1 + 2 * KSL + 2 * VSL + 8;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
-  __host__ __device__ static constexpr uint32_t s_col(int u) { return H + u * 2 * BN; }
-  __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + u * 2 * BN + BN; }
+  static_assert(alloc <= 232448, "shared memory per CTA");
+  __host__ __device__ static constexpr uint32_t s_col(int u) { return H + u * BN; }
+  __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + NBS * BN + u * BN; }
 };
 
 template <int H, int BN_>
 __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<H, BN_>;
-  constexpr int HC = C::HC, BN = C::BN, NBUF = C::NBUF, KSL = C::KSL, VSL = C::VSL;
+  constexpr int HC = C::HC, BN = C::BN, NBS = C::NBS, NBP = C::NBP, KSL = C::KSL, VSL = C::VSL;
+  // Hand-off barriers form a ring of two, tile n using entry n % 2 with parity (n / 2) & 1.
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
@@ -309,8 +318,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       // dQ(m) += dS(m) K(m); the HC chunks of K(m) sit in consecutive ring
       // slots, so one N = H product per 16 keys.
       auto issue_dq = [&](int m) -> bool {
-        const int u = m % NBUF;
-        if (!mbar_wait(ds_full(u), (m / NBUF) & 1, ab)) return false;
+        const int u = m % NBS;
+        if (!mbar_wait(ds_full(m & 1), (m >> 1) & 1, ab)) return false;
         tc_fence_after();
         const int slot0 = (m * HC) % KSL;
         const uint64_t b0 = sdesc_add(dkm, slot0 * C::KV_CHUNK);
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           mma_ts(tmem, tmem + C::s_col(u) + kk * 8, sdesc_add(b0, kk * 2048), id_q,
                  (m > 0 || kk > 0) ? 1u : 0u);
         for (int c = 0; c < HC; ++c) mma_commit(kempty(slot0 + c));
-        mma_commit(dq_done(u));
+        mma_commit(dq_done(m & 1));
         return true;
       };
       for (int jt = 0; jt < jr.y && ok; ++jt) {
@@ -328,8 +337,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
         }
-        const int u = n % NBUF;
-        // S columns of buffer u held dS(n-NBUF), read by dQ(n-NBUF), which this
+        const int u = n % NBS;
+        // S columns of buffer u held dS(n-NBS), read by dQ(n-NBS), which this
         // thread issued earlier (tcgen05.mma ops of one thread run in order).
         for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = (uint32_t)n * HC + c;
@@ -343,11 +352,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
                    (c > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(sdp_full(u));
-        if (n >= NBUF - 1 && !issue_dq(n - (NBUF - 1))) { ok = false; break; }
+        mma_commit(sdp_full(n & 1));
+        if (n >= NBS - 1 && !issue_dq(n - (NBS - 1))) { ok = false; break; }
         ++n;
       }
-      for (int m = n - (NBUF - 1); ok && m < n; ++m)
+      for (int m = n - (NBS - 1); ok && m < n; ++m)
         if (m >= 0 && !issue_dq(m)) ok = false;
       if (!ok) {
         mma_commit(teardown(0));
@@ -368,10 +377,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           if (!mbar_wait(q_full(), 0, ab)) { ok = false; break; }
           waited_q = true;
         }
-        const int u = n % NBUF;
-        // dP columns of buffer u are free once the softmax side has read dP(n-NBUF)
+        const int u = n % NBP;
+        // dP columns of buffer u are free once the softmax side has read dP(n-NBP)
         // (it signals ds_full after reading).
-        if (n >= NBUF && !mbar_wait(ds_full(u), ((n / NBUF) - 1) & 1, ab)) { ok = false; break; }
+        if (n >= NBP && !mbar_wait(ds_full((n - NBP) & 1), ((n - NBP) >> 1) & 1, ab)) { ok = false; break; }
         tc_fence_after();
         for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = (uint32_t)n * HC + c;
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           mma_commit(vempty(slot));
         }
         if (!ok) break;
-        mma_commit(sdp_full(u));
+        mma_commit(sdp_full(n & 1));
         ++n;
       }
       if (!ok) {
@@ -410,14 +419,14 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       if (jt < jr.x) continue;
       const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
-      const int u = n % NBUF;
-      if (!warp_wait(sdp_full(u), (n / NBUF) & 1, ab)) { ok = false; break; }
+      const int us = n % NBS, up = n % NBP;
+      if (!warp_wait(sdp_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t sv[32], pv[32];
-        tmem_ld32(tmem + lane_base + C::s_col(u) + c * 32, sv);
-        tmem_ld32(tmem + lane_base + C::dp_col(u) + c * 32, pv);
+        tmem_ld32(tmem + lane_base + C::s_col(us) + c * 32, sv);
+        tmem_ld32(tmem + lane_base + C::dp_col(up) + c * 32, pv);
         tmem_wait_ld();
         float* s = reinterpret_cast<float*>(sv);
         if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, jt * BN + c * 32);
@@ -431,16 +440,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           ds[i] = pack_bf16x2(d0, d1);
         }
         // dS (bf16, 2 per column) overwrites S columns already read.
-        tmem_st16(tmem + lane_base + C::s_col(u) + c * 16, ds);
+        tmem_st16(tmem + lane_base + C::s_col(us) + c * 16, ds);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_full(u));
+      mbar_arrive(ds_full(n & 1));
       ++n;
     }
     // dQ in bf16 is staged in the Q tile's shared memory (every MMA is done)
     // with the Q box's swizzled layout and written by TMA stores.
-    const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) % NBUF), ((n - 1) / NBUF) & 1, ab);
+    const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab);
     if (have) tc_fence_after();
 #pragma unroll 1
     for (int c = 0; c < H; c += 32) {
