@@ -28,7 +28,9 @@ namespace {
 // dK/dV: warps 0-3 and 7-10 softmax side (two per TMEM lane quadrant, one per
 // half of the key columns), 4 producer, 5-6 MMA issuers.
 constexpr int kThreads = 352;
-constexpr int kDqThreads = 256;  // dQ: 4 softmax-side warps, K producer, two MMA issuers, V producer
+// dQ: warps 0-3 and 8-11 softmax side (two per TMEM lane quadrant, one per half
+// of the key columns), 4 K producer, 5-6 MMA issuers, 7 V producer.
+constexpr int kDqThreads = 384;
 constexpr uint32_t kQChunk = 128 * 128;  // [128 rows x 64 dims] bf16
 constexpr float kLog2e = 1.4426950408889634f;
 enum : int { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
@@ -184,6 +186,11 @@ struct DqCfg {
   static constexpr uint32_t alloc = misc_off + 64 + 1024;
   static_assert(alloc <= 232448, "shared memory per CTA");
   __host__ __device__ static constexpr uint32_t s_col(int u) { return H + u * BN; }
+  // Column (within an S buffer) of dS for keys [32 c, 32 c + 32): the keys of
+  // each half of the tile are packed at the start of that half's S columns.
+  __host__ __device__ static constexpr uint32_t ds_col(int c) {
+    return (c / (BN / 64)) * (BN / 2) + (c % (BN / 64)) * 16;
+  }
   __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + NBS * BN + u * BN; }
 };
 
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     for (int s = 0; s < VSL; ++s) { mbar_init(vfull(s), 1); mbar_init(vempty(s), 1); }
     for (int u = 0; u < 2; ++u) {
       mbar_init(sdp_full(u), 2);  // S (issuer A) and dP (issuer B)
-      mbar_init(ds_full(u), kRows);
+      mbar_init(ds_full(u), 2 * kRows);
       mbar_init(dq_done(u), 1);
     }
     mbar_init(teardown(0), 1);
@@ -325,8 +332,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
         const uint64_t b0 = sdesc_add(dkm, slot0 * C::KV_CHUNK);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem, tmem + C::s_col(u) + kk * 8, sdesc_add(b0, kk * 2048), id_q,
-                 (m > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem, tmem + C::s_col(u) + C::ds_col(kk / 2) + (kk & 1) * 8, sdesc_add(b0, kk * 2048),
+                 id_q, (m > 0 || kk > 0) ? 1u : 0u);
         for (int c = 0; c < HC; ++c) mma_commit(kempty(slot0 + c));
         mma_commit(dq_done(m & 1));
         return true;
@@ -404,11 +411,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       }
     }
   } else {
-    // softmax-side: thread r owns packed query row r
-    const int r = tid, g = r / Tb, t = t0 + (r - g * Tb);
+    // softmax side: packed query row r sits in TMEM lane r; the two warps of a
+    // lane quadrant split the key columns (and, in the epilogue, the head dims)
+    const int quad = warp & 3, half = warp >= 8 ? 1 : 0;
+    const int r = quad * 32 + lane, g = r / Tb, t = t0 + (r - g * Tb);
     const bool valid = t < a.T;  // rows past T (ragged last tile) are inert
     const long row = ((long)bk * a.G + g) * a.T + t;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float lse = valid ? a.lse[row] : -INFINITY;
     const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
     const float Dr = valid ? a.delta[row] : 0.f;
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       if (!warp_wait(sdp_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         uint32_t sv[32], pv[32];
         tmem_ld32(tmem + lane_base + C::s_col(us) + c * 32, sv);
         tmem_ld32(tmem + lane_base + C::dp_col(up) + c * 32, pv);
@@ -439,8 +448,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
           const float d1 = p1 * (__uint_as_float(pv[2 * i + 1]) - Dr);
           ds[i] = pack_bf16x2(d0, d1);
         }
-        // dS (bf16, 2 per column) overwrites S columns already read.
-        tmem_st16(tmem + lane_base + C::s_col(us) + c * 16, ds);
+        // dS (bf16, 2 per column) overwrites S columns this warp has read: the
+        // half's dS goes to the start of the half's own S columns (the other
+        // warp of the quadrant is still reading its half).
+        tmem_st16(tmem + lane_base + C::s_col(us) + C::ds_col(c), ds);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -452,7 +463,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab);
     if (have) tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < H; c += 32) {
+    for (int c = half * (H / 2); c < (half + 1) * (H / 2); c += 32) {
       uint32_t v[32];
       if (have) {
         tmem_ld32(tmem + lane_base + c, v);
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(chunk + sw128_offset(r, u0 + i)) = pk[i];
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, kRows);
+    named_bar_sync(1, 2 * kRows);
     if (tid == 0) {
       for (int c = 0; c < HC; ++c) tma_store_4d(&a.tm_dq, sbase + C::q_off + c * kQChunk, c * 64, t0, 0, bk);
       bulk_commit();
