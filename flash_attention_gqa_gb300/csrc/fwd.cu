@@ -553,8 +553,9 @@ struct PFwdSmem {
   static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[2][kMaxKvTiles]
   static constexpr uint32_t bar_off = sched_off + 2 * kMaxKvTiles * 2;
   // q_full[2], sched_full[2], item_free[2], then the Bars block (full, empty,
-  // s_full, p_full, pv_done, teardown), then the O += P V issuer's teardown
-  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7 + 1;
+  // s_full, p_full, pv_done, teardown), the O += P V issuer's teardown, and
+  // o_staged
+  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7 + 1 + 1;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, item info[2][4]
   static constexpr uint32_t bytes = misc_off + 64;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -575,6 +576,10 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
   auto item_free = [&](int b) { return pb + 8 * (4 + b); };
   Bars bars{pb + 8 * 6};
   const uint32_t teardown_pv = pb + 8 * (6 + 1 + 2 * kSlots + 7);
+  // every softmax thread has staged its row of O / l: the storing thread waits
+  // on it with a bound (a named barrier could not give up if a warp aborted
+  // before reaching it)
+  const uint32_t o_staged = pb + 8 * (6 + 1 + 2 * kSlots + 7 + 1);
   auto sched = [&](int b) { return reinterpret_cast<uint16_t*>(sm + L::sched_off) + b * kMaxKvTiles; };
   auto q_tile = [&](int b) { return L::q_off + (uint32_t)b * HC * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
@@ -610,6 +615,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
     }
     mbar_init(bars.teardown(), 1);
     mbar_init(teardown_pv, 1);
+    mbar_init(o_staged, kRows);
     fence_barrier_init();
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
@@ -884,8 +890,9 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       if (valid) a.lse[((long)bk * a.G + g) * a.T + t] = lse_row;
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, kRows);
+      mbar_arrive(o_staged);
       if (tid == 0) {
+        if (!mbar_wait(o_staged, k & 1, ab)) { ok = false; break; }
         for (int c = 0; c < HC; ++c)
           tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, t0, 0, bk);
         bulk_commit();
