@@ -42,9 +42,9 @@ L2_BYTES = 129 * 2**20
 # by kernel name; valid only while the kernel source hashes to `src_sha`.
 NCU_TRAFFIC = {
     # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
-    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 274370000, "src_sha": "a1b019ab124a584e"},
-    "fa_bwd_dq_kernel": {"bytes_per_launch": 191350000, "src_sha": "a1b019ab124a584e"},
-    "fa_fwd_kernel": {"bytes_per_launch": 111020000, "src_sha": "ff8487c7a750f28e"},
+    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 327960000, "src_sha": "ee1f7d8d237d4247"},
+    "fa_bwd_dq_kernel": {"bytes_per_launch": 191280000, "src_sha": "ee1f7d8d237d4247"},
+    "fa_fwd_kernel": {"bytes_per_launch": 111250000, "src_sha": "f8478581664149d1"},
 }
 
 
