@@ -48,6 +48,7 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "fa_set_bwd_kv_rows": (_I, [ctypes.c_int]),
+    "fa_set_bwd_q_splits": (_I, [ctypes.c_int]),
     "fa_set_fwd_schedule": (_I, [ctypes.c_int]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_sm_count": (_I, []),
@@ -197,6 +198,11 @@ def fa_set_fwd_schedule(mode: int) -> int:
 def fa_set_bwd_kv_rows(rows: int) -> int:
     """Backward KV tile size for H = 128: 0 chooses per call, 64 / 128 force it."""
     return int(load().fa_set_bwd_kv_rows(int(rows)))
+
+
+def fa_set_bwd_q_splits(n: int) -> int:
+    """dK/dV Q-range split on grids smaller than the GPU: 0 chooses per call, 1..4 force it."""
+    return int(load().fa_set_bwd_q_splits(int(n)))
 
 
 def fa_selftest_wait_timeout(stream=None) -> int:

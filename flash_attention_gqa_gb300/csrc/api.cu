@@ -25,6 +25,7 @@ using fa::kRows;
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_bwd_kv_rows{0};  // 0: chosen per call; 64 / 128: forced where valid
+std::atomic<int> g_bwd_q_splits{0};  // 0: chosen per call; 1..4: forced where a split can apply
 std::atomic<int> g_fwd_schedule{0};  // 0: chosen per call; 1: CTA per Q tile; 2: persistent
 
 uint64_t wait_limit() {
@@ -252,16 +253,19 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int32_t* s
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H) {
   if (B <= 0 || K <= 0 || G <= 0 || T <= 0 || S < 0) return 0;
   if (check_shapes(B, K, G, T, S, H, 0, nullptr, nullptr) != FA_OK) return 0;
-  return fa::bwd_workspace_bytes(B, K, G, T, S, H);
+  return fa::bwd_workspace(B, K, G, T, S, H, fa_device_sm_count()).total;
 }
 
 namespace {
 
-// Shared body of fa_bwd and fa_bwd_stage: stage < 0 runs every stage.
+// Shared body of fa_bwd and fa_bwd_stage: stage < 0 runs every stage.  The
+// workspace must hold the base part; the Q-range split of a dK/dV grid smaller
+// than the GPU runs where allow_split and the workspace also holds the split part.
 int bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, const int32_t* seg_q, const int32_t* seg_kv, int causal,
              const fa::BlockMask& bm, void* dq, void* dk, void* dv, void* workspace,
-             size_t workspace_bytes, int B, int K, int G, int T, int S, int H, void* stream) {
+             size_t workspace_bytes, int B, int K, int G, int T, int S, int H, void* stream,
+             bool allow_split) {
   if (stage < -1 || stage > 2) return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
@@ -275,15 +279,16 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
                  !aligned16(dv)))
     return FA_ERR_INVALID_ARG;
   if (H == 64) return FA_ERR_UNSUPPORTED;
-  const size_t need = fa_bwd_workspace_size(B, K, G, T, S, H);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
-                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+  const int sms = fa_device_sm_count();
+  const fa::BwdWorkspace wl = fa::bwd_workspace(B, K, G, T, S, H, sms);
+  if ((long)B * K * G * T > 0 && (workspace == nullptr || workspace_bytes < wl.base ||
+                                  (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return FA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long rows = (long)B * K * G * T;
   const int BK = B * K;
   const int forced = g_bwd_kv_rows.load();
-  const int kvr = (H == 128 && forced != 0) ? forced : fa::bwd_kv_rows(H, B, K, S, fa_device_sm_count());
+  const int kvr = (H == 128 && forced != 0) ? forced : fa::bwd_kv_rows(H, B, K, S, sms);
   if (BK == 0) return FA_OK;
   if (rows == 0 || S == 0) {
     // No query rows or no keys: every gradient is zero.
@@ -311,13 +316,27 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.n_qtiles = (T + kRows / G - 1) / (kRows / G);
   a.n_kvtiles = (S + kvr - 1) / kvr;
   a.kv_rows = kvr;
+  const long dkdv_ctas = (long)BK * a.n_kvtiles;
+  // Split counters exist wherever the workspace holds the split part; stage 0
+  // zeroes them then (the last CTA of each KV tile re-zeroes its own after use).
+  const bool split_ok = allow_split && wl.partials > 0 && workspace_bytes >= wl.total && dkdv_ctas < sms;
+  int* counters = split_ok ? reinterpret_cast<int*>(static_cast<char*>(workspace) + wl.counters) : nullptr;
+  a.q_splits = 1;
+  if (split_ok) {
+    const int fs = g_bwd_q_splits.load();
+    a.q_splits = fs != 0 ? fs : fa::bwd_q_splits(dkdv_ctas, sms);
+  }
+  if (a.q_splits > 1) {
+    a.dkv_count = counters;
+    a.dkv_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.partials);
+  }
   a.bm = bm;
   a.err = error_word();
   a.wait_limit_ns = wait_limit();
   if (!a.err) return FA_ERR_CUDA;
   cudaError_t e = cudaSuccess;
   if (stage < 0 || stage == 0) {
-    e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, st);
+    e = fa::launch_bwd_preprocess(o, dO, delta, rows, H, counters, (int)dkdv_ctas, st);
     if (e == cudaSuccess) e = fa::launch_seg_ranges(a, st);
   }
   if (e == cudaSuccess && (stage < 0 || stage == 1)) e = fa::launch_bwd_dkdv(a, st);
@@ -335,7 +354,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int K, int G, int T,
            int S, int H, void* stream) {
   return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
-                  workspace, workspace_bytes, B, K, G, T, S, H, stream);
+                  workspace, workspace_bytes, B, K, G, T, S, H, stream, true);
 }
 
 int fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -348,7 +367,7 @@ int fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, co
   const int rc = make_block_mask(&bm, block_class, partial_index, partial_bits, mask_heads, K, G, T, S);
   if (rc != FA_OK) return rc;
   return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, bm, dq, dk, dv, workspace,
-                  workspace_bytes, B, K, G, T, S, H, stream);
+                  workspace_bytes, B, K, G, T, S, H, stream, true);
 }
 
 int fa_block_mask_build(const uint8_t* dense, int heads, int T, int S, uint8_t* block_class,
@@ -404,7 +423,7 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const v
                  int B, int K, int G, int T, int S, int H, void* stream) {
   if (stage < 0) return FA_ERR_INVALID_ARG;
   return bwd_impl(stage, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
-                  workspace, workspace_bytes, B, K, G, T, S, H, stream);
+                  workspace, workspace_bytes, B, K, G, T, S, H, stream, true);
 }
 
 // ------------------------------------------------------------------------
@@ -438,12 +457,13 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    void* stream) {
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
-  if (fa_bwd_workspace_size(B, K, G, T, S, H) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
+  // Only the base part (D rows, range table) lives in the scratch: no Q-range split here.
+  if (fa::bwd_workspace(B, K, G, T, S, H, 0).base > (size_t)FA_NOALLOC_SCRATCH_BYTES)
     return FA_ERR_UNSUPPORTED;
   void* scratch = noalloc_scratch_address();
   if (scratch == nullptr) return FA_ERR_CUDA;
   return bwd_impl(-1, q, k, v, o, lse, dO, seg_q, seg_kv, causal, fa::BlockMask{}, dq, dk, dv,
-                  scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES, B, K, G, T, S, H, stream);
+                  scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES, B, K, G, T, S, H, stream, false);
 }
 
 int fa_check_status(void* stream) {
@@ -478,6 +498,12 @@ int fa_set_wait_limit_ns(uint64_t ns) {
 int fa_set_bwd_kv_rows(int rows) {
   if (rows != 0 && rows != 64 && rows != 128) return FA_ERR_INVALID_ARG;
   g_bwd_kv_rows.store(rows);
+  return FA_OK;
+}
+
+int fa_set_bwd_q_splits(int n) {
+  if (n < 0 || n > fa::kMaxQSplits) return FA_ERR_INVALID_ARG;
+  g_bwd_q_splits.store(n);
   return FA_OK;
 }
 

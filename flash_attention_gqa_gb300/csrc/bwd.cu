@@ -17,6 +17,7 @@
 // The two gradient passes recompute S and dP (7 tile products instead of 5)
 // and in exchange need no atomics: every output element is written once by
 // one CTA, so the result is deterministic.
+#include <algorithm>
 #include <cuda_bf16.h>
 #include "block_mask.cuh"
 #include "kernels.h"
@@ -494,6 +495,128 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
   if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
 }
 
+// ====================================================== dK/dV epilogue
+// Run by the 8 softmax-side warps (256 threads) of a dK/dV CTA: TMEM lanes
+// carry the head dim (thread r of a quadrant pair owns dims r and 128 + r),
+// columns the keys (`half` selects this warp's half of them).  Without a split
+// (one CTA per KV tile) dV, dK go straight to bf16.  With the Q range of each
+// KV tile split over q_splits CTAs, each CTA stores its fp32 partial sums, and
+// the last CTA of the tile to finish (one atomic count per tile; no CTA ever
+// waits for another) adds the q_splits partials in split order and stores
+// bf16, so the result does not depend on which CTA finishes last.
+// have == false: this CTA contributes zeros.
+template <int H, int BN, bool SPLIT>
+__device__ __forceinline__ void dkdv_epilogue(const BwdArgs& a, uint32_t tmem_dv, uint32_t tmem_dk,
+                                              int r, int half, bool have, int jt, int split, int bk,
+                                              volatile int* last_flag) {
+  constexpr int HH = H / 128;
+  const int s0 = jt * BN;
+  __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
+  __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
+  if constexpr (!SPLIT) {
+#pragma unroll 1
+    for (int h = 0; h < HH; ++h) {
+      const int hd = h * 128 + r;
+#pragma unroll 1
+      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
+        uint32_t vv[32], kv[32];
+        if (have) {
+          tmem_ld32(tmem_dv + h * BN + c, vv);
+          tmem_ld32(tmem_dk + h * BN + c, kv);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
+            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
+            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+          }
+        }
+      }
+    }
+  } else {
+    const int NS = a.q_splits;
+    constexpr long kTile = (long)BN * H;  // floats of one partial dV (or dK) tile
+    const long BKn = (long)a.B * a.K;
+    auto part = [&](int p) { return a.dkv_part + (((long)jt * NS + p) * BKn + bk) * 2 * kTile; };
+    float* mine = part(split);
+#pragma unroll 1
+    for (int h = 0; h < HH; ++h) {
+      const int hd = h * 128 + r;
+#pragma unroll 1
+      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
+        uint32_t vv[32], kv[32];
+        if (have) {
+          tmem_ld32(tmem_dv + h * BN + c, vv);
+          tmem_ld32(tmem_dk + h * BN + c, kv);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          mine[(long)(c + k) * H + hd] = __uint_as_float(vv[k]);
+          mine[kTile + (long)(c + k) * H + hd] = __uint_as_float(kv[k]);
+        }
+      }
+    }
+    __threadfence();  // this CTA's partial is visible before its count
+    named_bar_sync(1, 2 * kRows);
+    if (r == 0 && half == 0) {
+      int* cnt = a.dkv_count + (long)jt * BKn + bk;
+      const bool last = atomicAdd(cnt, 1) == NS - 1;
+      if (last) atomicExch(cnt, 0);  // every CTA of the tile has counted: ready for the next call
+      *last_flag = last ? 1 : 0;
+    }
+    named_bar_sync(1, 2 * kRows);
+    if (*last_flag == 0) return;
+    __threadfence();
+    // 16 keys at a time: each partial's 32 values are loaded before any is
+    // added, then added in split order.
+#pragma unroll 1
+    for (int h = 0; h < HH; ++h) {
+      const int hd = h * 128 + r;
+#pragma unroll 1
+      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 16) {
+        float sv[16], sk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) { sv[k] = 0.f; sk[k] = 0.f; }
+#pragma unroll 1
+        for (int p = 0; p < NS; ++p) {
+          const float* src = part(p) + (long)c * H + hd;
+          float lv[16], lk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            lv[k] = __ldcg(src + (long)k * H);
+            lk[k] = __ldcg(src + kTile + (long)k * H);
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) { sv[k] += lv[k]; sk[k] += lk[k]; }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          if (s0 + c + k < a.S) {
+            dv[(long)(c + k) * H + hd] = __float2bfloat16(sv[k]);
+            dk[(long)(c + k) * H + hd] = __float2bfloat16(sk[k]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// The Q tiles [lo, hi) of KV tile jt's sweep that CTA `split` of q_splits takes:
+// equal shares of the tiles from the first one the causal bound lets see the tile.
+__device__ __forceinline__ int2 split_qrange(int qt_begin, int n_qtiles, int split, int n_splits) {
+  const int len = max(0, n_qtiles - qt_begin);
+  return make_int2(qt_begin + (int)((long)len * split / n_splits),
+                   qt_begin + (int)((long)len * (split + 1) / n_splits));
+}
+
 // ================================================================ dK/dV
 // One Q stage (H = 256: a second 64 KB Q tile does not fit next to K, V, dO, P
 // and dS).  S(i+1) follows dK^T(i), which reads the only Q buffer.
@@ -521,7 +644,7 @@ struct Dkv1Cfg {
   static constexpr uint32_t dp_col = 2 * HH * BN + BN;
 };
 
-template <int H, int BN_>
+template <int H, int BN_, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_constant__ BwdArgs a) {
   using C = Dkv1Cfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN;
@@ -544,9 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Tb = kRows / a.G;
-  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head first.
-  const int BKn = a.B * a.K;
-  const int jt = (int)(blockIdx.x / BKn);
+  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head
+  // first; with SPLIT the q_splits CTAs of a KV tile split its Q range.
+  const int BKn = a.B * a.K, NS = SPLIT ? a.q_splits : 1;
+  const int jt = (int)(blockIdx.x / (BKn * NS));
+  const int split = SPLIT ? (int)(blockIdx.x / BKn) % NS : 0;
   const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
   // The dQ kernel reads nothing this kernel writes: let it be scheduled on SMs
   // this grid frees in its tail (it is launched with programmatic serialization).
@@ -554,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
   const int s0 = jt * BN;
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
-  const int qt_begin = causal_first_qtile(a, s0, Tb);
+  const int2 qsw = split_qrange(causal_first_qtile(a, s0, Tb), a.n_qtiles, split, NS);
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -574,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int2 qrng = nonempty_range(qt_begin, a.n_qtiles, reinterpret_cast<int*>(sm + C::misc_off + 8),
+  const int2 qrng = nonempty_range(qsw.x, qsw.y, reinterpret_cast<int*>(sm + C::misc_off + 8),
                                    [&](int qt) { return tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN); });
 
   if (warp == 4) {
@@ -746,31 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
     const bool have = i > 0 && ok && warp_wait(q_empty(HH - 1), (i - 1) & 1, ab) &&
                       warp_wait(do_empty(HH - 1), (i - 1) & 1, ab);
     if (have) tc_fence_after();
-    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
-    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
-#pragma unroll 1
-    for (int h = 0; h < HH; ++h) {
-      const int hd = h * 128 + r;
-#pragma unroll 1
-      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
-        uint32_t vv[32], kv[32];
-        if (have) {
-          tmem_ld32(tmem + lane_base + C::dv_col + h * BN + c, vv);
-          tmem_ld32(tmem + lane_base + C::dk_col + h * BN + c, kv);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
-            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
-            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
-          }
-        }
-      }
-    }
+    dkdv_epilogue<H, BN, SPLIT>(a, tmem + lane_base + C::dv_col, tmem + lane_base + C::dk_col, r, half,
+                                have, jt, split, bk, reinterpret_cast<volatile int*>(sm + C::misc_off + 16));
   }
   tc_fence_before();
   __syncthreads();
@@ -811,7 +913,7 @@ struct DkvCfg {
   static constexpr uint32_t dp_col = 2 * HH * BN + BN;
 };
 
-template <int H, int BN_>
+template <int H, int BN_, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkvCfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN, QB = C::QB;
@@ -835,9 +937,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Tb = kRows / a.G;
-  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head first.
-  const int BKn = a.B * a.K;
-  const int jt = (int)(blockIdx.x / BKn);
+  // Flat grid, KV-tile major: early (causally heaviest) KV tiles of every head
+  // first; with SPLIT the q_splits CTAs of a KV tile split its Q range.
+  const int BKn = a.B * a.K, NS = SPLIT ? a.q_splits : 1;
+  const int jt = (int)(blockIdx.x / (BKn * NS));
+  const int split = SPLIT ? (int)(blockIdx.x / BKn) % NS : 0;
   const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
   // The dQ kernel reads nothing this kernel writes: let it be scheduled on SMs
   // this grid frees in its tail (it is launched with programmatic serialization).
@@ -845,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   const int s0 = jt * BN;
   const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
   const int2* kr = qr + (long)a.B * a.n_qtiles;
-  const int qt_begin = causal_first_qtile(a, s0, Tb);
+  const int2 qsw = split_qrange(causal_first_qtile(a, s0, Tb), a.n_qtiles, split, NS);
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -871,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int2 qrng = nonempty_range(qt_begin, a.n_qtiles, reinterpret_cast<int*>(sm + C::misc_off + 8),
+  const int2 qrng = nonempty_range(qsw.x, qsw.y, reinterpret_cast<int*>(sm + C::misc_off + 8),
                                    [&](int qt) { return tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN); });
 
   if (warp == 4) {
@@ -1098,31 +1202,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
                       wait_halves<HH>([&](int h) { return q_empty(lq, h); }, ((i - 1) / QB) & 1, ab) &&
                       wait_halves<HH>(do_empty, (i - 1) & 1, ab);
     if (have) tc_fence_after();
-    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
-    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
-#pragma unroll 1
-    for (int h = 0; h < HH; ++h) {
-      const int hd = h * 128 + r;
-#pragma unroll 1
-      for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
-        uint32_t vv[32], kv[32];
-        if (have) {
-          tmem_ld32(tmem + lane_base + C::dv_col + h * BN + c, vv);
-          tmem_ld32(tmem + lane_base + C::dk_col + h * BN + c, kv);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) { vv[k] = 0; kv[k] = 0; }
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
-            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
-            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
-          }
-        }
-      }
-    }
+    dkdv_epilogue<H, BN, SPLIT>(a, tmem + lane_base + C::dv_col, tmem + lane_base + C::dk_col, r, half,
+                                have, jt, split, bk, reinterpret_cast<volatile int*>(sm + C::misc_off + 16));
   }
   tc_fence_before();
   __syncthreads();
@@ -1137,8 +1218,10 @@ constexpr int kPreSteps = 4;
 template <int H>
 __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                       const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
-                                      long rows) {
+                                      long rows, int* __restrict__ zero, int n_zero) {
   constexpr int TPR = H / 8, RPW = 32 / TPR;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const long warp_id = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const long row0 = warp_id * kPreSteps * RPW + lane / TPR;
@@ -1223,43 +1306,60 @@ cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous
   return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H, BN>, a);
 }
 
-template <int H, int BN>
+template <int H, int BN, bool SPLIT>
 cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H, BN>, DkvCfg<H, BN>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H, BN, SPLIT>, DkvCfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<H, BN><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, DkvCfg<H, BN>::alloc, st>>>(a);
+  fa_bwd_dkdv_kernel<H, BN, SPLIT><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K), kThreads,
+                                     DkvCfg<H, BN>::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int H, int BN>
+template <int H, int BN, bool SPLIT>
 cudaError_t launch_dkdv1_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dkdv1_kernel<H, BN>, Dkv1Cfg<H, BN>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dkdv1_kernel<H, BN, SPLIT>, Dkv1Cfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv1_kernel<H, BN><<<dim3(a.n_kvtiles * a.B * a.K), kThreads, Dkv1Cfg<H, BN>::alloc, st>>>(a);
+  fa_bwd_dkdv1_kernel<H, BN, SPLIT><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K), kThreads,
+                                      Dkv1Cfg<H, BN>::alloc, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H) {
-  const size_t d = ((size_t)B * K * G * T * sizeof(float) + 255) & ~(size_t)255;
+BwdWorkspace bwd_workspace(int B, int K, int G, int T, int S, int H, int sm_count) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t d = up((size_t)B * K * G * T * sizeof(float));
   const size_t tb = kRows / G, kvr = kMinBwdKvRows;
   const size_t nq = (T + tb - 1) / tb, nk = (S + kvr - 1) / kvr;
-  const size_t r = ((size_t)B * (nq + nk) * sizeof(int2) + 255) & ~(size_t)255;
-  return d + r;
+  const size_t r = up((size_t)B * (nq + nk) * sizeof(int2));
+  BwdWorkspace w{0, 0, d + r, d + r};
+  // Every KV tile size the backward may pick for H: the largest split part.
+  size_t cnt = 0, part = 0;
+  for (int rows = 64; rows <= (H == 128 ? 128 : 64); rows *= 2) {
+    const long ctas = (long)B * K * ((S + rows - 1) / rows);
+    if (ctas <= 0 || ctas >= sm_count) continue;
+    cnt = std::max(cnt, up((size_t)ctas * sizeof(int)));
+    part = std::max(part, (size_t)kMaxQSplits * ctas * 2 * rows * H * sizeof(float));
+  }
+  if (part > 0) {
+    w.counters = w.base;
+    w.partials = w.base + cnt;
+    w.total = w.partials + up(part);
+  }
+  return w;
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
-                                  cudaStream_t st) {
+                                  int* zero, int n_zero, cudaStream_t st) {
   const int warps = 8;
   auto go = [&](auto kern, int tpr) {
     const long rows_per_block = (long)warps * kPreSteps * (32 / tpr);
     const long blocks = (rows + rows_per_block - 1) / rows_per_block;
     kern<<<(unsigned)blocks, warps * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(o),
                                                   reinterpret_cast<const __nv_bfloat16*>(dO), delta,
-                                                  rows);
+                                                  rows, zero, zero ? n_zero : 0);
   };
   switch (H) {
     case 128: go(bwd_preprocess_kernel<128>, 16); break;
@@ -1284,9 +1384,13 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
-  if (a.H == 128 && a.kv_rows == 128) return launch_dkdv_h<128, 128>(a, st);
-  if (a.H == 128 && a.kv_rows == 64) return launch_dkdv_h<128, 64>(a, st);
-  if (a.H == 256 && a.kv_rows == 64) return launch_dkdv1_h<256, 64>(a, st);
+  const bool split = a.q_splits > 1;
+  if (a.H == 128 && a.kv_rows == 128)
+    return split ? launch_dkdv_h<128, 128, true>(a, st) : launch_dkdv_h<128, 128, false>(a, st);
+  if (a.H == 128 && a.kv_rows == 64)
+    return split ? launch_dkdv_h<128, 64, true>(a, st) : launch_dkdv_h<128, 64, false>(a, st);
+  if (a.H == 256 && a.kv_rows == 64)
+    return split ? launch_dkdv1_h<256, 64, true>(a, st) : launch_dkdv1_h<256, 64, false>(a, st);
   return cudaErrorNotSupported;
 }
 

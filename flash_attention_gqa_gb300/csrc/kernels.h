@@ -58,14 +58,18 @@ struct BwdArgs {
   int n_qtiles;        // T / (128 / G)
   int n_kvtiles;       // S / kv_rows
   int kv_rows;         // keys per KV tile of the backward kernels (64 or 128)
+  int q_splits;        // CTAs sharing one KV tile's Q range in dK/dV (1: no split)
+  float* dkv_part;     // q_splits > 1: fp32 partial dV, dK per dK/dV CTA [CTA][2][kv_rows][H]
+  int* dkv_count;      // q_splits > 1: finished CTAs per (KV tile, b*K); zero between calls
   BlockMask bm;
   uint32_t* err;
   uint64_t wait_limit_ns;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st, int schedule);
+// Also zeroes n_zero ints at zero (the dK/dV split counters; may be null).
 cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, long rows, int H,
-                                  cudaStream_t st);
+                                  int* zero, int n_zero, cudaStream_t st);
 cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st);
 // overlap_previous: launch with programmatic stream serialization so the grid
@@ -88,7 +92,33 @@ inline int bwd_kv_rows(int H, int B, int K, int S, int sm_count) {
 }
 constexpr int kMinBwdKvRows = 64;  // the workspace's range table is sized for it
 
-// Backward workspace: fp32 D rows, then per-tile segment-id ranges.
-size_t bwd_workspace_bytes(int B, int K, int G, int T, int S, int H);
+// Q-range split of the dK/dV grid.  With fewer dK/dV CTAs than SMs, the Q
+// tiles of each KV tile are dealt to q_splits CTAs (causal masks make the
+// first KV tiles' sweeps the longest, so one CTA per KV tile leaves most SMs
+// idle while those finish).  The count in 1..kMaxQSplits minimising waves /
+// splits, ties to the larger; 1 when the grid already fills the GPU.
+constexpr int kMaxQSplits = 4;
+inline int bwd_q_splits(long ctas, int sm_count) {
+  if (ctas <= 0 || ctas >= sm_count) return 1;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int n = 1; n <= kMaxQSplits; ++n) {
+    const double cost = (double)((ctas * n + sm_count - 1) / sm_count) / n;
+    if (cost <= best_cost) { best_cost = cost; best = n; }
+  }
+  return best;
+}
+
+// Backward workspace: fp32 D rows, then per-tile segment-id ranges (the base
+// part), then, where a Q-range split can apply (a dK/dV grid smaller than
+// sm_count for some KV tile size), the split counters and kMaxQSplits fp32
+// partial dK/dV tiles per dK/dV CTA.
+struct BwdWorkspace {
+  size_t counters;  // offset of the split counters (0 where no split can apply)
+  size_t partials;  // offset of the partial tiles
+  size_t base;      // bytes without the split part
+  size_t total;     // bytes with it
+};
+BwdWorkspace bwd_workspace(int B, int K, int G, int T, int S, int H, int sm_count);
 
 }  // namespace fa

@@ -137,7 +137,11 @@ int fa_block_mask_build(const uint8_t* dense, int heads, int T, int S,
                         int64_t* n_partial);
 
 /* Bytes of device workspace fa_bwd needs for these sizes (a multiple of 256;
-   0 for empty or unsupported sizes). */
+   0 for empty or unsupported sizes), on the current device.  Where the dK/dV
+   grid (one CTA per KV tile and b*K) is smaller than the GPU, the size
+   includes the split part: kernel counters and fp32 partial dK/dV tiles for up
+   to 4 CTAs per KV tile.  fa_bwd runs with less, down to the D rows and range
+   table, but then without the Q-range split. */
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
 
 /*
@@ -148,8 +152,12 @@ size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
  * The pages give no backward; this is the textbook derivative of the forward
  * definition above.  `o` and `lse` must be those fa_fwd produced for the same
  * inputs.  `workspace` (>= fa_bwd_workspace_size bytes, 256-byte aligned)
- * holds the fp32 D rows and per-tile segment-id ranges; its contents on
- * entry do not matter.
+ * holds the fp32 D rows and per-tile segment-id ranges and, for small grids,
+ * the split part; its contents on entry do not matter.
+ * Where the dK/dV grid is smaller than the GPU, the Q tiles of each KV tile are
+ * dealt to up to 4 CTAs (fa_set_bwd_q_splits).  Each stores fp32 partial dK,
+ * dV.  The last of them to finish adds the partials in a fixed order, so the
+ * result stays deterministic.
  * Supported head dims: 128 and 256.
  */
 int fa_bwd(const void* q, const void* k, const void* v,
@@ -182,14 +190,17 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v,
  * device memory themselves: for example a plugin running inside a host
  * application that owns every device allocation and offers no allocator
  * hook, or a runtime whose rules forbid allocating after start-up.  It
- * computes exactly what fa_bwd computes and calls no cudaMalloc, cudaFree or
- * other allocating routine.  The pages have no counterpart to this call.
+ * computes what fa_bwd computes and calls no cudaMalloc, cudaFree or
+ * other allocating routine.  It never splits the dK/dV grid's Q ranges (the
+ * partial tiles would not fit its scratch), so on grids smaller than the GPU
+ * its dK and dV can differ from fa_bwd's in the last bits (fp32 summation
+ * order).  The pages have no counterpart to this call.
  *
  * The scratch (fp32 D rows plus per-tile segment ranges, the same data fa_bwd
  * keeps in its workspace) is one fixed array of FA_NOALLOC_SCRATCH_BYTES in
  * the library's device memory, present on every GPU that loads the library
  * until the process exits.  Sizes whose scratch would not fit
- * (fa_bwd_workspace_size(...) > FA_NOALLOC_SCRATCH_BYTES, i.e. roughly
+ * (D rows and range table over FA_NOALLOC_SCRATCH_BYTES, i.e. roughly
  * B*K*G*T > 2 million query rows) are rejected with FA_ERR_UNSUPPORTED before
  * anything is enqueued.
  *
@@ -230,6 +241,18 @@ int fa_set_wait_limit_ns(uint64_t ns);
  * fp32 summation order.  Returns FA_ERR_INVALID_ARG for any other value.
  */
 int fa_set_bwd_kv_rows(int rows);
+
+/*
+ * Q-range split of the dK/dV grid, for backward calls made after this one:
+ * 0 (default) chooses per call, 1..4 forces that many CTAs per KV tile.  Either
+ * applies only where the dK/dV grid is smaller than the GPU and the workspace
+ * holds the split part (fa_bwd_workspace_size); elsewhere there is one CTA per
+ * KV tile.  The default takes the count in 1..4 that minimises (waves of the
+ * split grid) / count, ties to the larger.  The result does not depend on the
+ * choice beyond fp32 summation order.  Returns FA_ERR_INVALID_ARG for any other
+ * value.
+ */
+int fa_set_bwd_q_splits(int n);
 
 /*
  * Forward grid for calls made after this one: 0 (default) chooses per call, 1

@@ -41,16 +41,41 @@ def test_status_strings(clib):
     assert binding.status_string(99) == "unknown status"
 
 
+def _split_part(B, K, S, H, sms):
+    """Bytes of the Q-range split part: counters and 4 fp32 partial dK/dV tiles
+    per dK/dV CTA, for the KV tile sizes (64, and 128 at H = 128) whose grid is
+    smaller than the GPU; the largest over them."""
+    up = lambda x: (x + 255) // 256 * 256
+    cnt = part = 0
+    for rows in ((64, 128) if H == 128 else (64,)):
+        ctas = B * K * -(-S // rows)
+        if 0 < ctas < sms:
+            cnt = max(cnt, up(ctas * 4))
+            part = max(part, 4 * ctas * 2 * rows * H * 4)
+    return cnt + up(part) if part else 0
+
+
 def test_workspace_size(clib):
+    sms = binding.load().fa_device_sm_count()   # 0 without a GPU: no split part
     # fp32 D rows, then one (min, max) int32 pair per (b, q tile) and (b, kv tile)
     n = binding.fa_bwd_workspace_size(1, 2, 8, 8192, 8192, 256)
-    assert n == 2 * 8 * 8192 * 4 + (8192 // 16 + 8192 // 64) * 8
+    assert n == 2 * 8 * 8192 * 4 + (8192 // 16 + 8192 // 64) * 8 + _split_part(1, 2, 8192, 256, sms)
     assert n % 256 == 0
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256 + \
+        _split_part(1, 1, 128, 128, sms)
     assert binding.fa_bwd_workspace_size(0, 1, 1, 128, 128, 128) == 0
     # ragged sizes: D rows rounded up to 256 B, then one range pair per tile
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256 + \
+        _split_part(1, 1, 130, 128, sms)
     assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 96) == 0      # H unsupported
+
+
+def test_split_part_layout():
+    # a 152-SM GPU: the T=1024 shape (B2 K2) splits at both KV tile sizes,
+    # the largest part being 4 x 64 CTAs x 2 x 64 x 128 fp32
+    assert _split_part(2, 2, 1024, 128, 152) == 256 + 4 * 64 * 2 * 64 * 128 * 4
+    assert _split_part(1, 2, 8192, 256, 152) == 0     # 256 CTAs fill the GPU
+    assert _split_part(1, 1, 128, 128, 0) == 0
 
 
 def _fwd(clib, *, q=16, k=16, v=16, sq=None, skv=None, causal=0, o=16, lse=16,
@@ -111,6 +136,13 @@ def test_bwd_kv_rows_setter(clib):
         assert binding.fa_set_bwd_kv_rows(bad) == binding.FA_ERR_INVALID_ARG
     for ok in (64, 128, 0):
         assert binding.fa_set_bwd_kv_rows(ok) == binding.FA_OK
+
+
+def test_bwd_q_splits_setter(clib):
+    for bad in (-1, 5, 64):
+        assert binding.fa_set_bwd_q_splits(bad) == binding.FA_ERR_INVALID_ARG
+    for ok in (1, 2, 3, 4, 0):
+        assert binding.fa_set_bwd_q_splits(ok) == binding.FA_OK
 
 
 def test_fwd_schedule_setter(clib):

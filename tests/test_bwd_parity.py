@@ -152,3 +152,78 @@ def test_h128_both_kv_tile_sizes(forced_kv_rows, name):
     seg = _doc_segs(c["B"], c["T"], 3) if c.pop("segs", False) else None
     run_case(c["B"], c["K"], c["G"], c["T"], c["S"], 128, causal=c["causal"], seg_q=seg,
              seg_kv=seg, seed=len(name) + forced_kv_rows)
+
+
+# --------------------------------- Q-range split of dK/dV grids under the GPU
+
+@pytest.fixture
+def forced_q_splits(request):
+    assert binding.fa_set_bwd_q_splits(request.param) == binding.FA_OK
+    yield request.param
+    binding.fa_set_bwd_q_splits(0)
+
+
+# Small grids, so the split applies; T > S and T < S give splits with no tile.
+Q_SPLIT_CASES = {
+    "causal_h128": dict(B=1, K=2, G=4, T=640, S=640, H=128, causal=True),
+    "causal_h256": dict(B=1, K=1, G=8, T=512, S=512, H=256, causal=True),
+    "full_ragged_h256": dict(B=1, K=1, G=4, T=333, S=300, H=256, causal=False),
+    "rect_causal_t_lt_s": dict(B=1, K=2, G=4, T=100, S=700, H=128, causal=True),
+    "rect_causal_t_gt_s": dict(B=1, K=1, G=8, T=700, S=200, H=256, causal=True),
+    "doc_segments": dict(B=2, K=1, G=4, T=640, S=640, H=128, causal=True, segs=True),
+}
+
+
+@pytest.mark.parametrize("forced_q_splits", [1, 2, 3, 4], indirect=True)
+@pytest.mark.parametrize("name", sorted(Q_SPLIT_CASES))
+def test_dkdv_q_splits(forced_q_splits, name):
+    c = dict(Q_SPLIT_CASES[name])
+    seg = _doc_segs(c["B"], c["T"], 5) if c.pop("segs", False) else None
+    run_case(c["B"], c["K"], c["G"], c["T"], c["S"], c["H"], causal=c["causal"], seg_q=seg,
+             seg_kv=seg, seed=len(name) + 10 * forced_q_splits)
+
+
+def _bwd_inputs(B, K, G, T, H, seed):
+    x = inputs.make_tensors(B, K, G, T, T, H, seed=seed, backward=True)
+    dev = torch.device("cuda")
+    q, k, v, dO = (t.to(dev) for t in (x.q, x.k, x.v, x.dO))
+    o, lse = binding.attention_forward(q, k, v, causal=True)
+    return q, k, v, o, lse, dO
+
+
+@pytest.mark.parametrize("H", [128, 256])
+def test_split_backward_is_repeatable_and_matches_unsplit(H):
+    q, k, v, o, lse, dO = _bwd_inputs(1, 2, 4, 1024, H, seed=23)
+    split = [binding.attention_backward(q, k, v, o, lse, dO, causal=True) for _ in range(2)]
+    for x1, x2 in zip(*split):
+        assert torch.equal(x1, x2)       # the partials are added in a fixed order
+    assert binding.fa_set_bwd_q_splits(1) == binding.FA_OK
+    try:
+        whole = binding.attention_backward(q, k, v, o, lse, dO, causal=True)
+    finally:
+        binding.fa_set_bwd_q_splits(0)
+    assert torch.equal(split[0][0], whole[0])    # dQ does not take part in the split
+    for name, a, b in zip(("dk", "dv"), split[0][1:], whole[1:]):
+        a, b = to_np(a), to_np(b)
+        # only the fp32 summation order differs: at most about one bf16 unit
+        assert np.linalg.norm(a - b) <= 2.0 ** -8 * np.linalg.norm(b), name
+
+
+def test_backward_runs_unsplit_in_a_base_size_workspace():
+    B, K, G, T, H = 1, 2, 4, 640, 128
+    q, k, v, o, lse, dO = _bwd_inputs(B, K, G, T, H, seed=29)
+    up = lambda n: (n + 255) // 256 * 256
+    base = up(B * K * G * T * 4) + up(B * (T // (128 // G) + -(-T // 64)) * 8)
+    assert binding.fa_bwd_workspace_size(B, K, G, T, T, H) > base   # the split part exists here
+    dev = q.device
+    outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    binding.fa_bwd(q, k, v, o, lse, dO, None, None, True, *outs,
+                   torch.empty(base, device=dev, dtype=torch.uint8))
+    assert binding.fa_check_status() == binding.FA_OK
+    assert binding.fa_set_bwd_q_splits(1) == binding.FA_OK
+    try:
+        whole = binding.attention_backward(q, k, v, o, lse, dO, causal=True)
+    finally:
+        binding.fa_set_bwd_q_splits(0)
+    for a, b in zip(outs, whole):
+        assert torch.equal(a, b)         # no split part: the one-CTA-per-KV-tile result
