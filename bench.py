@@ -42,9 +42,12 @@ L2_BYTES = 129 * 2**20
 # by kernel name; valid only while the kernel source hashes to `src_sha`.
 NCU_TRAFFIC = {
     # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
-    "fa_bwd_dkdv_kernel": {"bytes_per_launch": 327960000, "src_sha": "ee1f7d8d237d4247"},
-    "fa_bwd_dq_kernel": {"bytes_per_launch": 191280000, "src_sha": "ee1f7d8d237d4247"},
-    "fa_fwd_kernel": {"bytes_per_launch": 111250000, "src_sha": "f8478581664149d1"},
+    # of each kernel; reported only for that workload and unchanged sources
+    "gqa_causal_h256_t8192": {
+        "fa_bwd_dkdv_kernel": {"bytes_per_launch": 273400000, "src_sha": "4b52371faedf9f19"},
+        "fa_bwd_dq_kernel": {"bytes_per_launch": 191360000, "src_sha": "4b52371faedf9f19"},
+        "fa_fwd_kernel": {"bytes_per_launch": 111140000, "src_sha": "f8478581664149d1"},
+    },
 }
 
 
@@ -404,7 +407,7 @@ def ours_arm(args, world, rank, local):
     timed_s = ms * args.steps / 1e3
     peak = burst if timed_s < 1.0 else sustained
     src_file = "fwd.cu" if top == "fa_fwd_kernel" else "bwd.cu"
-    tr = NCU_TRAFFIC.get(top)
+    tr = NCU_TRAFFIC.get(w.name, {}).get(top)
     traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(src_file) else None
     if w.kind == "decode":
         # memory-bound: K and V are read once, q / o / lse move once
