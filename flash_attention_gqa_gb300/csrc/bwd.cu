@@ -330,12 +330,30 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
         if (!mbar_wait(ds_full(m & 1), (m >> 1) & 1, ab)) return false;
         tc_fence_after();
         const int slot0 = (m * HC) % KSL;
-        const uint64_t b0 = sdesc_add(dkm, slot0 * C::KV_CHUNK);
+        if constexpr (H == 256) {
+          // Two N = 128 products, one per half of the head dims: the K chunks of
+          // the first half are released while the second half still runs, so
+          // the next K tile's first chunks (the ring holds only two tiles at
+          // H = 256) start loading earlier.
+          constexpr uint32_t id_h = idesc_bf16(128, 128, false, true);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem, tmem + C::s_col(u) + C::ds_col(kk / 2) + (kk & 1) * 8, sdesc_add(b0, kk * 2048),
-                 id_q, (m > 0 || kk > 0) ? 1u : 0u);
-        for (int c = 0; c < HC; ++c) mma_commit(kempty(slot0 + c));
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t bh = sdesc_add(dkm, (slot0 + 2 * hh) * C::KV_CHUNK);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tmem + hh * 128, tmem + C::s_col(u) + C::ds_col(kk / 2) + (kk & 1) * 8,
+                     sdesc_add(bh, kk * 2048), id_h, (m > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(kempty(slot0 + 2 * hh));
+            mma_commit(kempty(slot0 + 2 * hh + 1));
+          }
+        } else {
+          const uint64_t b0 = sdesc_add(dkm, slot0 * C::KV_CHUNK);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem, tmem + C::s_col(u) + C::ds_col(kk / 2) + (kk & 1) * 8, sdesc_add(b0, kk * 2048),
+                   id_q, (m > 0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < HC; ++c) mma_commit(kempty(slot0 + c));
+        }
         mma_commit(dq_done(m & 1));
         return true;
       };
