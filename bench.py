@@ -44,9 +44,9 @@ NCU_TRAFFIC = {
     # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
     # of each kernel; reported only for that workload and unchanged sources
     "gqa_causal_h256_t8192": {
-        "fa_bwd_dkdv_kernel": {"bytes_per_launch": 273400000, "src_sha": "4b52371faedf9f19"},
-        "fa_bwd_dq_kernel": {"bytes_per_launch": 191360000, "src_sha": "4b52371faedf9f19"},
-        "fa_fwd_kernel": {"bytes_per_launch": 111140000, "src_sha": "f8478581664149d1"},
+        "fa_bwd_dkdv_kernel": {"bytes_per_launch": 230500000, "src_sha": "c7d9f8e70cff12c0"},
+        "fa_bwd_dq_kernel": {"bytes_per_launch": 191420000, "src_sha": "c7d9f8e70cff12c0"},
+        "fa_fwd_kernel": {"bytes_per_launch": 110910000, "src_sha": "f8478581664149d1"},
     },
 }
 
