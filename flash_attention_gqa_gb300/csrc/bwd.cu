@@ -3,20 +3,24 @@
 // The pages give no backward; this is the derivative of the forward written
 // out (P = exp(L - lse), dP = dO V^T, dS = P (dP - D), dq = dS K,
 // dk = sum_g dS^T q, dv = sum_g P^T dO) in four launches:
-//   1. preprocess   D[row] = sum_h dO * o (fp32), one warp per row
+//   1. preprocess   D[row] = sum_h dO * o (fp32), H / 8 lanes per row
 //   2. seg ranges   per-tile [min, max] segment ids (only with SegmentIds)
 //   3. dK/dV        one CTA per (kv tile, b*K): K and V stay in shared memory,
 //                   the non-empty Q tiles (G heads packed, 128 rows) stream by;
 //                   S = Q K^T and dP = dO V^T recomputed in TMEM, P and dS
 //                   written to shared memory, and dV^T += dO^T P,
 //                   dK^T += Q^T dS accumulated in TMEM with the head dim on the
-//                   128 lanes (so H = 256 fits in tensor memory).
+//                   128 lanes (so H = 256 fits in tensor memory).  Where that
+//                   grid is smaller than the GPU, up to 4 CTAs share a KV
+//                   tile's Q tiles and the last to finish adds their fp32
+//                   partial sums in a fixed order.
 //   4. dQ           one CTA per (Q tile, b*K): Q and dO stay in shared memory,
 //                   the non-empty KV tiles stream by; dS goes to TMEM as the A
 //                   operand of dQ += dS K.
 // The two gradient passes recompute S and dP (7 tile products instead of 5)
-// and in exchange need no atomics: every output element is written once by
-// one CTA, so the result is deterministic.
+// and in exchange need no atomic accumulation: every output element is
+// written once, by one CTA, from sums taken in a fixed order, so the result
+// is deterministic.
 #include <algorithm>
 #include <cuda_bf16.h>
 #include "block_mask.cuh"
