@@ -39,7 +39,8 @@ DEFAULT_WORKLOAD = "gqa_causal_h256_t8192"
 L2_BYTES = 129 * 2**20
 
 # DRAM traffic per launch of the roofline kernel from one ncu capture, keyed
-# by kernel name; valid only while the kernel source hashes to `src_sha`.
+# by workload and kernel name; valid only while the kernel source's code (its
+# comments aside) hashes to `src_sha`.
 NCU_TRAFFIC = {
     # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
     # of each kernel; reported only for that workload and unchanged sources
