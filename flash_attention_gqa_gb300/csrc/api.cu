@@ -324,7 +324,8 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.q_splits = 1;
   if (split_ok) {
     const int fs = g_bwd_q_splits.load();
-    a.q_splits = fs != 0 ? fs : fa::bwd_q_splits(dkdv_ctas, sms);
+    const bool uneven = causal || seg_q != nullptr || bm.cls != nullptr;
+    a.q_splits = fs != 0 ? fs : fa::bwd_q_splits(dkdv_ctas, sms, uneven);
   }
   if (a.q_splits > 1) {
     a.dkv_count = counters;

@@ -93,18 +93,20 @@ inline int bwd_kv_rows(int H, int B, int K, int S, int sm_count) {
 constexpr int kMinBwdKvRows = 64;  // the workspace's range table is sized for it
 
 // Q-range split of the dK/dV grid.  With fewer dK/dV CTAs than SMs, the Q
-// tiles of each KV tile are dealt to q_splits CTAs (causal masks make the
-// first KV tiles' sweeps the longest, so one CTA per KV tile leaves most SMs
-// idle while those finish).  The count in 1..kMaxQSplits minimising waves /
-// splits, ties to the larger; 1 when the grid already fills the GPU.
+// tiles of each KV tile are dealt to q_splits CTAs.  The count in
+// 1..kMaxQSplits minimising waves / splits.  Ties go to the larger count when
+// the sweeps are uneven (causal, segment ids or a block mask: the first KV
+// tiles' sweeps are the longest, and splitting shortens them) and to the
+// smaller otherwise (equal sweeps: more CTAs only add waves and fixed costs).
+// 1 when the grid already fills the GPU.
 constexpr int kMaxQSplits = 4;
-inline int bwd_q_splits(long ctas, int sm_count) {
+inline int bwd_q_splits(long ctas, int sm_count, bool uneven) {
   if (ctas <= 0 || ctas >= sm_count) return 1;
   int best = 1;
   double best_cost = 1e30;
   for (int n = 1; n <= kMaxQSplits; ++n) {
     const double cost = (double)((ctas * n + sm_count - 1) / sm_count) / n;
-    if (cost <= best_cost) { best_cost = cost; best = n; }
+    if (cost < best_cost || (uneven && cost == best_cost)) { best_cost = cost; best = n; }
   }
   return best;
 }
