@@ -413,14 +413,18 @@ def ours_arm(args, world, rank, local):
     src_file = "fwd.cu" if top == "fa_fwd_kernel" else "bwd.cu"
     tr = NCU_TRAFFIC.get(w.name, {}).get(top)
     traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(src_file) else None
-    if w.kind == "decode":
-        # memory-bound: K and V are read once, q / o / lse move once
-        fbytes = 2 * (x.k.numel() + x.v.numel() + 2 * x.q.numel()) + 4 * lse.numel()
+    # forward algorithmic bytes: q, k, v, o and lse move once
+    fbytes = 2 * (x.k.numel() + x.v.numel() + 2 * x.q.numel()) + 4 * lse.numel()
+    ridge = peak * 1e12 / (hbm * 1e9)   # FLOP per byte where the two roofs meet
+    if w.kind == "decode" or (not w.backward and fwd_flop / fbytes < ridge):
+        # below the ridge: the roofline bound is HBM
         achieved = fbytes / (per["fa_fwd_kernel"] * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "fa_fwd_kernel (split-KV x%d) + merge" % n_splits,
+        kname = ("fa_fwd_kernel (split-KV x%d) + merge" % n_splits) if n_splits > 1 else "fa_fwd_kernel"
+        roofline = {"bound": "hbm", "kernel": kname,
                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": None,
-                    "algorithmic_bytes": fbytes, "peak_source": f"{src} HBM copy",
+                    "algorithmic_bytes": fbytes, "intensity_flop_per_byte": round(fwd_flop / fbytes, 1),
+                    "ridge_flop_per_byte": round(ridge, 1), "peak_source": f"{src} HBM copy",
                     "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
     else:
         achieved = kflop[top] / (per[top] * 1e-3) / 1e12
