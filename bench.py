@@ -102,7 +102,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        out = os.environ.get("FA_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out, f"clocks_rank{index}.csv")
 
     def start(self):
         try:
