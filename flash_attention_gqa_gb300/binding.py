@@ -49,6 +49,7 @@ SIGNATURES = {
     "fa_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "fa_set_bwd_kv_rows": (_I, [ctypes.c_int]),
     "fa_set_bwd_q_splits": (_I, [ctypes.c_int]),
+    "fa_bwd_plan": (_I, [ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)] * 2),
     "fa_set_fwd_schedule": (_I, [ctypes.c_int]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_sm_count": (_I, []),
@@ -203,6 +204,14 @@ def fa_set_bwd_kv_rows(rows: int) -> int:
 def fa_set_bwd_q_splits(n: int) -> int:
     """dK/dV Q-range split on grids smaller than the GPU: 0 chooses per call, 1..4 force it."""
     return int(load().fa_set_bwd_q_splits(int(n)))
+
+
+def fa_bwd_plan(B, K, G, T, S, H, causal, masked, sm_count):
+    """(status, kv_rows, q_splits) the backward would choose with the default knobs."""
+    kv, qs = ctypes.c_int(0), ctypes.c_int(0)
+    rc = int(load().fa_bwd_plan(B, K, G, T, S, H, int(bool(causal)), int(bool(masked)), sm_count,
+                                ctypes.byref(kv), ctypes.byref(qs)))
+    return rc, kv.value, qs.value
 
 
 def fa_selftest_wait_timeout(stream=None) -> int:

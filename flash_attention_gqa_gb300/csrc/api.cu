@@ -508,6 +508,19 @@ int fa_set_bwd_q_splits(int n) {
   return FA_OK;
 }
 
+int fa_bwd_plan(int B, int K, int G, int T, int S, int H, int causal, int masked, int sm_count,
+                int* kv_rows, int* q_splits) {
+  if (kv_rows == nullptr || q_splits == nullptr || sm_count < 0) return FA_ERR_INVALID_ARG;
+  const int rc = check_shapes(B, K, G, T, S, H, causal, nullptr, nullptr);
+  if (rc != FA_OK) return rc;
+  if (H == 64) return FA_ERR_UNSUPPORTED;
+  const int kvr = fa::bwd_kv_rows(H, B, K, S, sm_count);
+  const long ctas = (long)B * K * ((S + kvr - 1) / kvr);
+  *kv_rows = kvr;
+  *q_splits = fa::bwd_q_splits(ctas, sm_count, causal != 0 || masked != 0);
+  return FA_OK;
+}
+
 int fa_set_fwd_schedule(int mode) {
   if (mode < 0 || mode > 2) return FA_ERR_INVALID_ARG;
   g_fwd_schedule.store(mode);

@@ -256,6 +256,17 @@ int fa_set_bwd_kv_rows(int rows);
 int fa_set_bwd_q_splits(int n);
 
 /*
+ * The backward's grid plan with the default knobs, on a GPU with sm_count SMs,
+ * for the shapes of an fa_bwd (masked != 0: segment ids or a block mask are
+ * given): *kv_rows = keys per KV tile (64 or 128), *q_splits = CTAs per KV tile
+ * of the dK/dV grid (1-4; used where the workspace holds the split part).  A
+ * host-only query: touches no device.  Returns FA_ERR_INVALID_ARG for null
+ * outputs or a negative sm_count, and the shape errors of fa_bwd.
+ */
+int fa_bwd_plan(int B, int K, int G, int T, int S, int H, int causal, int masked,
+                int sm_count, int* kv_rows, int* q_splits);
+
+/*
  * Forward grid for calls made after this one: 0 (default) chooses per call, 1
  * launches one CTA per Q tile, 2 launches one persistent CTA per SM that walks
  * the Q tiles, the next tile's schedule, Q copy and first products overlapping
