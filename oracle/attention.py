@@ -13,9 +13,9 @@ float64, on the bf16-rounded inputs:
     naive attention?", danielwatson6.github.io/fa/fa.html: the naive GQA
     attention with pre-scaled queries and the bkgth,bksh->bkgts contraction).
   * Mask    M[t,s] = (s <= t if causal) and (seg_q[b,t] == seg_kv[b,s] if
-    segment ids are given) -- SegmentIds docs ("Only the token with the same id
-    can attend", pallas_operations.flash_attention.tpu.jax_flash_attn_tpu,
-    section "SegmentIds"); causal as the lower-triangular mask of the axlearn
+    segment ids are given) -- SegmentIds docs (a token attends only to tokens
+    carrying the same segment id; pallas_operations.flash_attention.tpu.
+    jax_flash_attn_tpu, section "SegmentIds"); causal as the lower-triangular mask of the axlearn
     PR "Optimize TPU Flash Attention (400x speed-up on 32k long context)".
   * Softmax over the kept keys with the maximum subtracted (the tutorial's
     "Chunked attention" section: softmax(l) = softmax(l + c)), then
@@ -34,7 +34,8 @@ Readings where the pages are silent (all listed with the design notes):
     (splash attention's MultiHeadMask / process_mask in the tutorial's
     "Our first kernel" baseline);
   * a query row with no kept key has O = 0, lse = -inf and contributes no
-    gradient ("only the same id can attend" leaves it nothing to attend to);
+    gradient (with attention limited to equal ids, such a row has nothing to
+    attend to);
   * natural exp/log throughout; lse is in natural-log units.
 
 Everything is blocked over query rows only, so long sequences fit in memory;
