@@ -278,7 +278,6 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   if (has_kv && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
                  !aligned16(dv)))
     return FA_ERR_INVALID_ARG;
-  if (H == 64) return FA_ERR_UNSUPPORTED;
   const int sms = fa_device_sm_count();
   const fa::BwdWorkspace wl = fa::bwd_workspace(B, K, G, T, S, H, sms);
   if ((long)B * K * G * T > 0 && (workspace == nullptr || workspace_bytes < wl.base ||
@@ -288,7 +287,7 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   const long rows = (long)B * K * G * T;
   const int BK = B * K;
   const int forced = g_bwd_kv_rows.load();
-  const int kvr = (H == 128 && forced != 0) ? forced : fa::bwd_kv_rows(H, B, K, S, sms);
+  const int kvr = (H <= 128 && forced != 0) ? forced : fa::bwd_kv_rows(H, B, K, S, sms);
   if (BK == 0) return FA_OK;
   if (rows == 0 || S == 0) {
     // No query rows or no keys: every gradient is zero.
@@ -307,8 +306,13 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
       !make_q_map(&a.tm_dq, dq, BK, G, T, H))
     return FA_ERR_CUDA;
   float* delta = static_cast<float*>(workspace);
+  // The range table starts at its own 256-byte boundary past the D rows (an
+  // offset of rows * 4 bytes would misalign its 8-byte pairs for odd row counts).
+  int2* ranges = reinterpret_cast<int2*>(static_cast<char*>(workspace) + wl.ranges);
+  if ((reinterpret_cast<uintptr_t>(ranges) & 7u) != 0) return FA_ERR_INVALID_ARG;
   a.lse = lse;
   a.delta = delta;
+  a.seg_ranges = ranges;
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.seg_q = seg_q; a.seg_kv = seg_kv;
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
@@ -513,7 +517,6 @@ int fa_bwd_plan(int B, int K, int G, int T, int S, int H, int causal, int masked
   if (kv_rows == nullptr || q_splits == nullptr || sm_count < 0) return FA_ERR_INVALID_ARG;
   const int rc = check_shapes(B, K, G, T, S, H, causal, nullptr, nullptr);
   if (rc != FA_OK) return rc;
-  if (H == 64) return FA_ERR_UNSUPPORTED;
   const int kvr = fa::bwd_kv_rows(H, B, K, S, sm_count);
   const long ctas = (long)B * K * ((S + kvr - 1) / kvr);
   *kv_rows = kvr;

@@ -230,9 +230,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
   const int qt = a.n_qtiles - 1 - (int)(blockIdx.x / BKn);
   const int bk = (int)(blockIdx.x % BKn), b = bk / a.K;
   const int t0 = qt * Tb;
-  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* qr = a.seg_ranges;  // read only when segment ids are given
   const int2* kr = qr + (long)a.B * a.n_qtiles;
-  // qr/kr are only read when segment ids are given (they live past D).
   const int jt_end = causal_kv_end(a, t0, Tb, BN);
 
   if (tid == 0) {
@@ -507,7 +506,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     fence_proxy_async_smem();
     named_bar_sync(1, 2 * kRows);
     if (tid == 0) {
-      for (int c = 0; c < HC; ++c) tma_store_4d(&a.tm_dq, sbase + C::q_off + c * kQChunk, c * 64, t0, 0, bk);
+      for (int c = 0; c < HC; ++c)  // (H = 64 runs as 128: its zero upper chunk is not stored)
+        if (c * 64 < a.H) tma_store_4d(&a.tm_dq, sbase + C::q_off + c * kQChunk, c * 64, t0, 0, bk);
       bulk_commit();
       bulk_wait_read0();
     }
@@ -533,12 +533,16 @@ __device__ __forceinline__ void dkdv_epilogue(const BwdArgs& a, uint32_t tmem_dv
                                               volatile int* last_flag) {
   constexpr int HH = H / 128;
   const int s0 = jt * BN;
-  __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * H;
-  __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * H;
+  // a.H <= H: with H = 64 the kernel runs as H = 128 over zero-filled upper
+  // dims, whose rows of dK^T / dV^T are zero and are not stored.
+  const int Hs = a.H;
+  __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dv) + ((long)bk * a.S + s0) * Hs;
+  __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dk) + ((long)bk * a.S + s0) * Hs;
   if constexpr (!SPLIT) {
 #pragma unroll 1
     for (int h = 0; h < HH; ++h) {
       const int hd = h * 128 + r;
+      if (hd >= Hs) continue;
 #pragma unroll 1
       for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 32) {
         uint32_t vv[32], kv[32];
@@ -553,8 +557,8 @@ __device__ __forceinline__ void dkdv_epilogue(const BwdArgs& a, uint32_t tmem_dv
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           if (s0 + c + k < a.S) {  // keys past S (ragged last tile) are not stored
-            dv[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(vv[k]));
-            dk[(long)(c + k) * H + hd] = __float2bfloat16(__uint_as_float(kv[k]));
+            dv[(long)(c + k) * Hs + hd] = __float2bfloat16(__uint_as_float(vv[k]));
+            dk[(long)(c + k) * Hs + hd] = __float2bfloat16(__uint_as_float(kv[k]));
           }
         }
       }
@@ -602,6 +606,7 @@ __device__ __forceinline__ void dkdv_epilogue(const BwdArgs& a, uint32_t tmem_dv
 #pragma unroll 1
     for (int h = 0; h < HH; ++h) {
       const int hd = h * 128 + r;
+      if (hd >= Hs) continue;
 #pragma unroll 1
       for (int c = half * BN / 2; c < (half + 1) * BN / 2; c += 16) {
         float sv[16], sk[16];
@@ -622,8 +627,8 @@ __device__ __forceinline__ void dkdv_epilogue(const BwdArgs& a, uint32_t tmem_dv
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           if (s0 + c + k < a.S) {
-            dv[(long)(c + k) * H + hd] = __float2bfloat16(sv[k]);
-            dk[(long)(c + k) * H + hd] = __float2bfloat16(sk[k]);
+            dv[(long)(c + k) * Hs + hd] = __float2bfloat16(sv[k]);
+            dk[(long)(c + k) * Hs + hd] = __float2bfloat16(sk[k]);
           }
         }
       }
@@ -699,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
   // this grid frees in its tail (it is launched with programmatic serialization).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int s0 = jt * BN;
-  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* qr = a.seg_ranges;  // read only when segment ids are given
   const int2* kr = qr + (long)a.B * a.n_qtiles;
   const int2 qsw = split_qrange(causal_first_qtile(a, s0, Tb), a.n_qtiles, split, NS);
 
@@ -969,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
   // this grid frees in its tail (it is launched with programmatic serialization).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int s0 = jt * BN;
-  const int2* qr = reinterpret_cast<const int2*>(a.delta + (long)a.B * a.K * a.G * a.T);
+  const int2* qr = a.seg_ranges;  // read only when segment ids are given
   const int2* kr = qr + (long)a.B * a.n_qtiles;
   const int2 qsw = split_qrange(causal_first_qtile(a, s0, Tb), a.n_qtiles, split, NS);
 
@@ -1356,14 +1361,15 @@ BwdWorkspace bwd_workspace(int B, int K, int G, int T, int S, int H, int sm_coun
   const size_t tb = kRows / G, kvr = kMinBwdKvRows;
   const size_t nq = (T + tb - 1) / tb, nk = (S + kvr - 1) / kvr;
   const size_t r = up((size_t)B * (nq + nk) * sizeof(int2));
-  BwdWorkspace w{0, 0, d + r, d + r};
+  BwdWorkspace w{d, 0, 0, d + r, d + r};
   // Every KV tile size the backward may pick for H: the largest split part.
   size_t cnt = 0, part = 0;
-  for (int rows = 64; rows <= (H == 128 ? 128 : 64); rows *= 2) {
+  const size_t Hk = H < 128 ? 128 : H;  // the kernels' head dim (H = 64 runs as 128)
+  for (int rows = 64; rows <= (H <= 128 ? 128 : 64); rows *= 2) {
     const long ctas = (long)B * K * ((S + rows - 1) / rows);
     if (ctas <= 0 || ctas >= sm_count) continue;
     cnt = std::max(cnt, up((size_t)ctas * sizeof(int)));
-    part = std::max(part, (size_t)kMaxQSplits * ctas * 2 * rows * H * sizeof(float));
+    part = std::max(part, (size_t)kMaxQSplits * ctas * 2 * rows * Hk * sizeof(float));
   }
   if (part > 0) {
     w.counters = w.base;
@@ -1384,6 +1390,7 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, l
                                                   rows, zero, zero ? n_zero : 0);
   };
   switch (H) {
+    case 64: go(bwd_preprocess_kernel<64>, 8); break;
     case 128: go(bwd_preprocess_kernel<128>, 16); break;
     case 256: go(bwd_preprocess_kernel<256>, 32); break;
     default: return cudaErrorNotSupported;
@@ -1393,7 +1400,7 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dO, float* delta, l
 
 cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
   if (a.seg_q == nullptr) return cudaSuccess;
-  int2* qr = reinterpret_cast<int2*>(const_cast<float*>(a.delta) + (long)a.B * a.K * a.G * a.T);
+  int2* qr = a.seg_ranges;
   int2* kr = qr + (long)a.B * a.n_qtiles;
   const int Tb = kRows / a.G;
   const long nq = (long)a.B * a.n_qtiles, nk = (long)a.B * a.n_kvtiles;
@@ -1405,11 +1412,16 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// H = 64 runs the H = 128 kernels: the TMA boxes of the upper 64 head dims lie
+// wholly past the tensors' last dim and arrive zero-filled, which adds zero to
+// S and dP and gives zero rows of dK^T, dV^T and zero dQ columns, none of
+// which is stored.
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
   const bool split = a.q_splits > 1;
-  if (a.H == 128 && a.kv_rows == 128)
+  const bool h128 = a.H == 128 || a.H == 64;
+  if (h128 && a.kv_rows == 128)
     return split ? launch_dkdv_h<128, 128, true>(a, st) : launch_dkdv_h<128, 128, false>(a, st);
-  if (a.H == 128 && a.kv_rows == 64)
+  if (h128 && a.kv_rows == 64)
     return split ? launch_dkdv_h<128, 64, true>(a, st) : launch_dkdv_h<128, 64, false>(a, st);
   if (a.H == 256 && a.kv_rows == 64)
     return split ? launch_dkdv1_h<256, 64, true>(a, st) : launch_dkdv1_h<256, 64, false>(a, st);
@@ -1417,8 +1429,9 @@ cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
-  if (a.H == 128 && a.kv_rows == 128) return launch_dq_h<128, 128>(a, st, overlap_previous);
-  if (a.H == 128 && a.kv_rows == 64) return launch_dq_h<128, 64>(a, st, overlap_previous);
+  const bool h128 = a.H == 128 || a.H == 64;
+  if (h128 && a.kv_rows == 128) return launch_dq_h<128, 128>(a, st, overlap_previous);
+  if (h128 && a.kv_rows == 64) return launch_dq_h<128, 64>(a, st, overlap_previous);
   if (a.H == 256 && a.kv_rows == 64) return launch_dq_h<256, 64>(a, st, overlap_previous);
   return cudaErrorNotSupported;
 }

@@ -48,6 +48,9 @@ struct BwdArgs {
   CUtensorMap tm_dq;   // dq as 4-D, same box as q (TMA store)
   const float* lse;    // [B*K, G, T]
   const float* delta;  // [B*K, G, T]  D = rowsum(dO * o)
+  // Per-tile [min, max] segment ids (read only with segment ids): B * n_qtiles
+  // Q-tile pairs, then B * n_kvtiles KV-tile pairs.  8-byte aligned.
+  int2* seg_ranges;
   void* dq;            // bf16 [B*K, G, T, H]
   void* dk;            // bf16 [B*K, S, H]
   void* dv;            // bf16 [B*K, S, H]
@@ -82,7 +85,7 @@ cudaError_t launch_split_combine(const float* part_o, const float* part_lse, int
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 // KV rows per tile of the backward kernels.  H = 256 always takes 64 (a
-// 128-key K/V pair does not fit in shared memory next to the Q/dO tiles); H =
+// 128-key K/V pair does not fit in shared memory next to the Q/dO tiles); H <=
 // 128 takes 128 unless that leaves the dK/dV grid (one CTA per KV tile and
 // b*K) smaller than the GPU, where 64-key tiles double its CTAs.
 inline int bwd_kv_rows(int H, int B, int K, int S, int sm_count) {
@@ -116,6 +119,7 @@ inline int bwd_q_splits(long ctas, int sm_count, bool uneven) {
 // sm_count for some KV tile size), the split counters and kMaxQSplits fp32
 // partial dK/dV tiles per dK/dV CTA.
 struct BwdWorkspace {
+  size_t ranges;    // offset of the segment-range table (256-byte aligned)
   size_t counters;  // offset of the split counters (0 where no split can apply)
   size_t partials;  // offset of the partial tiles
   size_t base;      // bytes without the split part

@@ -38,7 +38,7 @@ enum {
   FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, one seg pointer without the
                                  other, misaligned pointer, workspace too small */
   FA_ERR_UNSUPPORTED = 2,     /* H not in {64,128,256}, G not a power of two <= 128,
-                                 S > 131072, B*K > 65535, backward with H == 64 */
+                                 S > 131072, B*K > 65535 */
   FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call or launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device wait ran out (kernel gave up) */
 };
@@ -158,7 +158,10 @@ size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
  * dealt to up to 4 CTAs (fa_set_bwd_q_splits).  Each stores fp32 partial dK,
  * dV.  The last of them to finish adds the partials in a fixed order, so the
  * result stays deterministic.
- * Supported head dims: 128 and 256.
+ * Head dims 64, 128 and 256.  H = 64 runs the H = 128 kernels: the upper 64
+ * head dims of every tile arrive zero-filled (their TMA boxes lie past the
+ * tensors' last dim), add nothing to S and dP, and their zero gradient rows
+ * are not stored; correct, at the tensor-core cost of H = 128.
  */
 int fa_bwd(const void* q, const void* k, const void* v,
            const void* o, const float* lse, const void* dO,
@@ -194,7 +197,8 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v,
  * other allocating routine.  It never splits the dK/dV grid's Q ranges (the
  * partial tiles would not fit its scratch), so on grids smaller than the GPU
  * its dK and dV can differ from fa_bwd's in the last bits (fp32 summation
- * order).  The pages have no counterpart to this call.
+ * order); with that split forced off in fa_bwd (fa_set_bwd_q_splits(1)) the
+ * two give the same bits.  The pages have no counterpart to this call.
  *
  * The scratch (fp32 D rows plus per-tile segment ranges, the same data fa_bwd
  * keeps in its workspace) is one fixed array of FA_NOALLOC_SCRATCH_BYTES in
@@ -234,7 +238,7 @@ const char* fa_status_string(int status);
 int fa_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Keys per KV tile of the backward kernels for H = 128 calls made after this
+ * Keys per KV tile of the backward kernels for H <= 128 calls made after this
  * one: 0 (default) chooses per call (128, or 64 when the dK/dV grid of
  * ceil(S/128)*B*K CTAs would not fill the GPU), 64 or 128 force that size.
  * H = 256 always uses 64.  The result does not depend on the choice beyond

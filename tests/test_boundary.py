@@ -43,15 +43,16 @@ def test_status_strings(clib):
 
 def _split_part(B, K, S, H, sms):
     """Bytes of the Q-range split part: counters and 4 fp32 partial dK/dV tiles
-    per dK/dV CTA, for the KV tile sizes (64, and 128 at H = 128) whose grid is
-    smaller than the GPU; the largest over them."""
+    per dK/dV CTA, for the KV tile sizes (64, and 128 at H <= 128) whose grid is
+    smaller than the GPU; the largest over them.  H = 64 runs the H = 128
+    kernels, so its partial tiles have 128 head dims."""
     up = lambda x: (x + 255) // 256 * 256
     cnt = part = 0
-    for rows in ((64, 128) if H == 128 else (64,)):
+    for rows in ((64, 128) if H <= 128 else (64,)):
         ctas = B * K * -(-S // rows)
         if 0 < ctas < sms:
             cnt = max(cnt, up(ctas * 4))
-            part = max(part, 4 * ctas * 2 * rows * H * 4)
+            part = max(part, 4 * ctas * 2 * rows * max(H, 128) * 4)
     return cnt + up(part) if part else 0
 
 
@@ -68,6 +69,9 @@ def test_workspace_size(clib):
     assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256 + \
         _split_part(1, 1, 130, 128, sms)
     assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 96) == 0      # H unsupported
+    # H = 64: D rows and range table as for any H, the split part at 128 head dims
+    assert binding.fa_bwd_workspace_size(2, 2, 4, 1024, 1024, 64) == 2 * 2 * 4 * 1024 * 4 + \
+        256 * ((2 * (1024 // 32 + 1024 // 64) * 8 + 255) // 256) + _split_part(2, 2, 1024, 64, sms)
 
 
 def test_split_part_layout():
@@ -110,7 +114,7 @@ def test_bwd_validation(clib):
     assert call(ws=0) == binding.FA_ERR_INVALID_ARG
     assert call(ws=272) == binding.FA_ERR_INVALID_ARG                 # not 256-aligned
     assert call(ws_bytes=16) == binding.FA_ERR_INVALID_ARG
-    assert call(H=64) == binding.FA_ERR_UNSUPPORTED
+    assert call(H=96) == binding.FA_ERR_UNSUPPORTED
 
 
 def test_splitkv_host_side(clib):
@@ -170,5 +174,8 @@ def test_bwd_plan(clib):
     assert plan(1, 140, 1, 64, 64, 256, 1, 0, 152) == (OK, 64, 4)
     # no SMs reported: nothing is split, H=128 keeps 128-key tiles
     assert plan(1, 1, 4, 128, 128, 128, 1, 0, 0) == (OK, 128, 1)
-    assert plan(1, 1, 4, 128, 128, 64, 1, 0, 152)[0] == binding.FA_ERR_UNSUPPORTED
+    # H = 64 follows the H = 128 rule (it runs the H = 128 kernels)
+    assert plan(2, 2, 4, 1024, 1024, 64, 1, 0, 152) == (OK, 64, 4)
+    assert plan(4, 8, 4, 4096, 4096, 64, 1, 1, 152) == (OK, 128, 1)
+    assert plan(1, 1, 4, 128, 128, 96, 1, 0, 152)[0] == binding.FA_ERR_UNSUPPORTED
     assert plan(1, 1, 4, 128, 128, 128, 1, 0, -1)[0] == binding.FA_ERR_INVALID_ARG

@@ -33,7 +33,7 @@ def run_case(B, K, G, T, S, H, causal=False, seg_q=None, seg_kv=None, seed=0):
     return (dq, dk, dv), g_ref, errs
 
 
-@pytest.mark.parametrize("H", [128, 256])
+@pytest.mark.parametrize("H", [64, 128, 256])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("causal", [False, True])
 def test_shapes(H, G, causal):
@@ -96,6 +96,18 @@ def test_ragged_segments():
     run_case(1, 1, 8, T, T + 5, 256, causal=False, seg_q=seg_q, seg_kv=seg_kv, seed=8)
 
 
+@pytest.mark.parametrize("H", [128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_odd_row_count_with_segments(H, causal):
+    # B*K*G*T = 77 rows: the segment-range table follows an odd number of fp32
+    # D rows in the workspace, so its 8-byte pairs need their own alignment
+    seg = inputs.document_segment_ids(1, 77, seed=9, lo=5, hi=30)
+    run_case(1, 1, 1, 77, 77, H, causal=causal, seg_q=seg, seg_kv=seg, seed=41 + H)
+    seg_q = inputs.random_segment_ids(1, 77, 3, seed=10)
+    seg_kv = inputs.random_segment_ids(1, 91, 3, seed=11)
+    run_case(1, 1, 1, 77, 91, H, causal=False, seg_q=seg_q, seg_kv=seg_kv, seed=43 + H)
+
+
 def test_causal_workload_h128_t1024_full():
     w = inputs.WORKLOADS["gqa_causal_h128_t1024"]
     run_case(w.B, w.K, w.G, w.T, w.S, w.H, causal=True, seed=w.seed)
@@ -112,15 +124,31 @@ def test_backward_is_deterministic():
         assert torch.equal(x1, x2)
 
 
-def test_h64_backward_is_rejected():
-    dev = torch.device("cuda")
-    q = torch.zeros(1, 1, 4, 128, 64, device=dev, dtype=torch.bfloat16)
-    k = torch.zeros(1, 1, 128, 64, device=dev, dtype=torch.bfloat16)
-    o, lse = binding.attention_forward(q, k, k)
-    rc = binding.fa_bwd(q, k, k, o, lse, q, None, None, False, torch.empty_like(q),
-                        torch.empty_like(k), torch.empty_like(k),
-                        torch.empty(4096, device=dev, dtype=torch.uint8), check=False)
-    assert rc == binding.FA_ERR_UNSUPPORTED
+# H = 64 runs the H = 128 kernels over zero-filled upper head dims: ragged
+# sizes, segment ids, both KV tile sizes and the dK/dV split must all hold.
+@pytest.mark.parametrize("T,S,causal", [(77, 77, True), (300, 300, False), (100, 300, True),
+                                        (1000, 1000, True)])
+def test_h64_ragged_and_rectangular(T, S, causal):
+    run_case(1, 2, 4, T, S, 64, causal=causal, seed=T + S + 64)
+
+
+def test_h64_segments():
+    seg = inputs.document_segment_ids(2, 640, seed=12, lo=40, hi=300)
+    run_case(2, 2, 4, 640, 640, 64, causal=True, seg_q=seg, seg_kv=seg, seed=64)
+    seg = inputs.random_segment_ids(1, 333, 3, seed=13)
+    run_case(1, 1, 8, 333, 333, 64, causal=False, seg_q=seg, seg_kv=seg, seed=65)
+
+
+@pytest.mark.parametrize("rows", [64, 128])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_h64_kv_tile_sizes_and_splits(rows, splits):
+    assert binding.fa_set_bwd_kv_rows(rows) == binding.FA_OK
+    assert binding.fa_set_bwd_q_splits(splits) == binding.FA_OK
+    try:
+        run_case(1, 2, 4, 640, 640, 64, causal=True, seed=rows + splits)
+    finally:
+        binding.fa_set_bwd_kv_rows(0)
+        binding.fa_set_bwd_q_splits(0)
 
 
 # ----------------------------------------------- both KV tile sizes at H = 128
