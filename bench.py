@@ -39,17 +39,39 @@ DEFAULT_WORKLOAD = "gqa_causal_h256_t8192"
 L2_BYTES = 129 * 2**20
 
 # DRAM traffic per launch of the roofline kernel from one ncu capture, keyed
-# by workload and kernel name; valid only while the kernel source's code (its
-# comments aside) hashes to `src_sha`.
-NCU_TRAFFIC = {
-    # one --metrics capture of the causal H=256, T=S=8192 step: mean of 16 launches
-    # of each kernel; reported only for that workload and unchanged sources
-    "gqa_causal_h256_t8192": {
-        "fa_bwd_dkdv_kernel": {"bytes_per_launch": 230500000, "src_sha": "f6ed718b77f6d535"},
-        "fa_bwd_dq_kernel": {"bytes_per_launch": 191420000, "src_sha": "f6ed718b77f6d535"},
-        "fa_fwd_kernel": {"bytes_per_launch": 110910000, "src_sha": "d2b8009a8cd7663c"},
-    },
-}
+# by workload and kernel label (as kernel_names() gives it); valid only while
+# the kernel source's code (its comments aside) hashes to `src_sha`.  Each
+# entry names the capture it comes from in `note`.
+NCU_TRAFFIC: dict = {}
+
+
+def kernel_names(w: inputs.Workload, n_splits: int, masked: bool) -> dict:
+    """Labels of the launches one step makes, as ncu names the kernels
+    (template arguments included), from the rules the library applies: the
+    persistent forward for H <= 128 without split-KV when the Q tiles
+    outnumber the SMs; the backward's KV tile size and dK/dV split from
+    fa_bwd_plan."""
+    from flash_attention_gqa_gb300 import binding
+    sms = binding.fa_device_sm_count()
+    items = -(-w.T // (128 // w.G)) * w.B * w.K
+    if n_splits > 1:
+        fwd = f"fa_fwd_kernel<{w.H}> (split-KV x{n_splits}) + split_combine_kernel<{w.H}>"
+    elif w.H <= 128 and items > sms:
+        fwd = f"fa_fwd_persistent_kernel<{w.H}>"
+    else:
+        fwd = f"fa_fwd_kernel<{w.H}>"
+    names = {"fwd": fwd}
+    if w.backward:
+        rc, kvr, qs = binding.fa_bwd_plan(w.B, w.K, w.G, w.T, w.S, w.H, w.causal,
+                                          masked or w.segments, sms)
+        assert rc == binding.FA_OK, binding.status_string(rc)
+        split = int(qs > 1)
+        dkdv = (f"fa_bwd_dkdv1_kernel<256, {kvr}, {split}>" if w.H == 256
+                else f"fa_bwd_dkdv_kernel<{max(w.H, 128)}, {kvr}, {split}>")
+        dq = f"fa_bwd_dq_kernel<{max(w.H, 128)}, {kvr}>"
+        pre = f"bwd_preprocess_kernel<{w.H}>" + (" + seg_ranges_kernel x2" if w.segments else "")
+        names.update(pre=pre, dkdv=dkdv, dq=dq, bwd=f"fa_bwd_masked: {pre} + {dkdv} + {dq}")
+    return names
 
 
 def parse_args():
@@ -360,29 +382,27 @@ def ours_arm(args, world, rank, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    if small:
-        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush()
-            step_ev[i][0].record(stream)
-            step()
-            step_ev[i][1].record(stream)
-    else:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step()
-        t_end.record(stream)
+    # every step between its own pair of events; the reported step time is the
+    # median over the timed steps (the mean is reported beside it)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start.record(stream)
+    for i in range(args.steps):
+        flush()
+        step_ev[i][0].record(stream)
+        step()
+        step_ev[i][1].record(stream)
+    t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     status = binding.fa_check_status(stream)
     assert status == binding.FA_OK, binding.status_string(status)
-    if small:
-        ms = reduce_max(sum(a_.elapsed_time(b_) for a_, b_ in step_ev) / args.steps, dev)
-    else:
-        ms = reduce_max(t_start.elapsed_time(t_end) / args.steps, dev)
+    step_ms = [a_.elapsed_time(b_) for a_, b_ in step_ev]
+    ms = reduce_max(statistics.median(step_ms), dev)
+    ms_mean = reduce_max(statistics.mean(step_ms), dev)
+    span_ms = reduce_max(t_start.elapsed_time(t_end), dev)
 
     # per-kernel device time: a second loop, stage by stage with CUDA events
     # between the launches (which also keeps dQ from overlapping dK/dV there)
@@ -392,35 +412,34 @@ def ours_arm(args, world, rank, local):
         flush()
         step(events[i])
     torch.cuda.synchronize()
-    per = {}
-    per["fa_fwd_kernel"] = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    if w.backward:
-        per["bwd_preprocess"] = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
-        per["fa_bwd_dkdv_kernel"] = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
-        per["fa_bwd_dq_kernel"] = statistics.mean(e[3].elapsed_time(e[4]) for e in events)
-    # algorithmic FLOPs each kernel performs: fwd = S and O products; dK/dV = S,
-    # dP, dV, dK products (2x fwd); dQ = S, dP, dQ products (1.5x fwd)
-    kflop = {"fa_fwd_kernel": fwd_flop, "fa_bwd_dkdv_kernel": 2.0 * fwd_flop,
-             "fa_bwd_dq_kernel": 1.5 * fwd_flop}
-    if meta is not None and w.backward:   # one timed block for the whole masked backward
-        per = {"fa_fwd_kernel": per["fa_fwd_kernel"],
-               "fa_bwd_masked (all stages)": per["bwd_preprocess"] + per["fa_bwd_dkdv_kernel"]
-               + per["fa_bwd_dq_kernel"]}
-        kflop = {"fa_fwd_kernel": fwd_flop}
+    med = lambda i, j: statistics.median(e[i].elapsed_time(e[j]) for e in events)
+    names = kernel_names(w, n_splits, meta is not None)
+    per = {names["fwd"]: med(0, 1)}
+    # algorithmic FLOPs each launch performs: fwd = S and O products; dK/dV = S,
+    # dP, dV, dK products (2x fwd); dQ = S, dP, dQ products (1.5x fwd); the
+    # backward as a whole counts 2.5x fwd
+    kflop = {names["fwd"]: fwd_flop}
+    if w.backward and meta is None:
+        per[names["pre"]] = med(1, 2)
+        per[names["dkdv"]] = med(2, 3)
+        per[names["dq"]] = med(3, 4)
+        kflop.update({names["dkdv"]: 2.0 * fwd_flop, names["dq"]: 1.5 * fwd_flop})
+    elif w.backward:   # the masked backward is one call: timed and counted as a whole
+        per[names["bwd"]] = med(1, 4)
+        kflop[names["bwd"]] = bwd_flop
     top = max((n for n in per if n in kflop), key=lambda n: per[n])
     burst, sustained, hbm, src = measured_peaks()
-    timed_s = ms * args.steps / 1e3
+    timed_s = span_ms / 1e3
     peak = burst if timed_s < 1.0 else sustained
-    src_file = "fwd.cu" if top == "fa_fwd_kernel" else "bwd.cu"
     tr = NCU_TRAFFIC.get(w.name, {}).get(top)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(src_file) else None
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(tr["src"]) else None
     # forward algorithmic bytes: q, k, v, o and lse move once
     fbytes = 2 * (x.k.numel() + x.v.numel() + 2 * x.q.numel()) + 4 * lse.numel()
     ridge = peak * 1e12 / (hbm * 1e9)   # FLOP per byte where the two roofs meet
     if w.kind == "decode" or (not w.backward and fwd_flop / fbytes < ridge):
         # below the ridge: the roofline bound is HBM
-        achieved = fbytes / (per["fa_fwd_kernel"] * 1e-3) / 1e9
-        kname = ("fa_fwd_kernel (split-KV x%d) + merge" % n_splits) if n_splits > 1 else "fa_fwd_kernel"
+        achieved = fbytes / (per[names["fwd"]] * 1e-3) / 1e9
+        kname = names["fwd"]
         roofline = {"bound": "hbm", "kernel": kname,
                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": None,
@@ -432,8 +451,12 @@ def ours_arm(args, world, rank, local):
         roofline = {"bound": "tensor", "kernel": top, "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": traffic,
+                    "traffic_source": (tr["note"] if traffic is not None else
+                                       "no ncu capture of this kernel's current code"),
+                    "algorithmic_flop": kflop[top],
                     "peak_source": f"{src} bf16 {'burst' if peak == burst else 'sustained'}",
-                    "per_kernel_ms": {n: round(t, 4) for n, t in per.items()}}
+                    "per_kernel_ms": {n: round(t, 4) for n, t in per.items()},
+                    "per_kernel_ms_stat": f"median of {n_k} steps, events between launches"}
 
     # end to end through the C ABI with host buffers: H2D inputs, D2H outputs
     host_in = [t.pin_memory() for t in (x.q, x.k, x.v) + ((x.dO,) if w.backward else ())]
@@ -529,14 +552,15 @@ def ours_arm(args, world, rank, local):
         "metric": METRIC,
         "value": round(world * step_flop / (ms * 1e-3) / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(ms, 4), "ms_per_step_stat": f"median of {args.steps} steps",
+        "ms_per_step_mean": round(ms_mean, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded; q pre-scaled by H^-1/2)",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "G": w.G, "T": w.T, "S": w.S,
                    "H": w.H, "causal": w.causal, "segments": w.segments,
                    "unmasked_frac": round(frac, 6), "fwd_flop": fwd_flop, "bwd_flop": bwd_flop,
-                   "fwd_tflops": round(fwd_flop / (per["fa_fwd_kernel"] * 1e-3) / 1e12, 1),
-                   "bwd_tflops": (round(bwd_flop / ((ms - per["fa_fwd_kernel"]) * 1e-3) / 1e12, 1)
+                   "fwd_tflops": round(fwd_flop / (per[names["fwd"]] * 1e-3) / 1e12, 1),
+                   "bwd_tflops": (round(bwd_flop / ((ms - per[names["fwd"]]) * 1e-3) / 1e12, 1)
                                   if w.backward else None),
                    "kind": w.kind, "split_kv": n_splits if n_splits > 1 else None,
                    "window": w.window or None,
@@ -544,7 +568,7 @@ def ours_arm(args, world, rank, local):
                    "l2": f"inputs+outputs {in_bytes / 2**20:.0f} MiB vs L2 {L2_BYTES / 2**20:.0f} MiB"
                          + (" (larger: no flush)" if not small else
                             f" (smaller: {2 * L2_BYTES / 2**20:.0f} MiB written between timed steps, "
-                            "each step timed by its own events)"),
+                            "outside the steps' events)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "e2e": {"value": round(world * step_flop / (e2e_best * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
