@@ -247,6 +247,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     mbar_init(teardown(0), 1);
     mbar_init(teardown(1), 1);
     fence_barrier_init();
+    // Q and dO at kernel entry: their latency overlaps set-up and classification
+    mbar_arrive_expect_tx(q_full(), 2 * HC * kQChunk);
+    for (int c = 0; c < HC; ++c) {
+      tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(), c * 64, t0, 0, bk);
+      tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, q_full(), c * 64, t0, 0, bk);
+    }
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
   tc_fence_before();
@@ -267,17 +273,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       bool ok = true;
       uint32_t seq = 0;  // chunk sequence number
       uint32_t k_issued = 0;
-      bool any = false;
       for (int jt = 0; jt < jr.y && ok; ++jt) {
         if (jt < jr.x || tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
-        if (!any) {
-          any = true;
-          mbar_arrive_expect_tx(q_full(), 2 * HC * kQChunk);
-          for (int c = 0; c < HC; ++c) {
-            tma_load_4d(sbase + C::q_off + c * kQChunk, &a.tm_q, q_full(), c * 64, t0, 0, bk);
-            tma_load_4d(sbase + C::do_off + c * kQChunk, &a.tm_do, q_full(), c * 64, t0, 0, bk);
-          }
-        }
         for (int c = 0; c < HC && ok; ++c) {
           const uint32_t sq = seq + c;
           const int slot = sq % KSL;
@@ -484,6 +481,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
     // with the Q box's swizzled layout and written by TMA stores.
     const bool have = n > 0 && ok && warp_wait(dq_done((n - 1) & 1), ((n - 1) >> 1) & 1, ab);
     if (have) tc_fence_after();
+    // The staging below overwrites the Q tile: with no product issued, nothing
+    // has waited for its copy yet.
+    if (n == 0) mbar_wait_teardown(q_full(), 0, a.wait_limit_ns);
 #pragma unroll 1
     for (int c = half * (H / 2); c < (half + 1) * (H / 2); c += 32) {
       uint32_t v[32];
@@ -723,6 +723,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
     mbar_init(teardown(1), 1);
     for (int c = 0; c < HC; ++c) { mbar_init(q_full(c), 1); mbar_init(do_full(c), 1); }
     fence_barrier_init();
+    // K and V at kernel entry: their latency overlaps set-up and classification
+    mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
+    for (int c = 0; c < HC; ++c) {
+      tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
+      tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
+    }
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
   tc_fence_before();
@@ -736,19 +742,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
     // Producer: K, V once; per Q tile, dO (released after dV^T) then Q
     // (released after dK^T), one barrier per 64-dim chunk.
     if (lane == 0) {
-      bool ok = true, any = false;
+      bool ok = true;
       int i = 0;
       uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
       for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
-        if (!any) {
-          any = true;
-          mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
-          for (int c = 0; c < HC; ++c) {
-            tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
-            tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
-          }
-        }
         issued = 0;
         for (int h = 0; h < HH && ok; ++h) {
           if (i > 0 && !mbar_wait(do_empty(h), (i - 1) & 1, ab)) { ok = false; break; }
@@ -904,6 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
     dkdv_epilogue<H, BN, SPLIT>(a, tmem + lane_base + C::dv_col, tmem + lane_base + C::dk_col, r, half,
                                 have, jt, split, bk, reinterpret_cast<volatile int*>(sm + C::misc_off + 16));
   }
+  if (tid == 0) mbar_wait_teardown(kv_full, 0, a.wait_limit_ns);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
@@ -999,6 +998,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       for (int qb = 0; qb < QB; ++qb) mbar_init(q_full(qb, c), 1);
     }
     fence_barrier_init();
+    // K and V at kernel entry: their latency overlaps set-up and classification
+    mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
+    for (int c = 0; c < HC; ++c) {
+      tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
+      tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
+    }
   }
   if (warp == 5) { tmem_alloc(smem_u32(tmem_slot), 512); tmem_relinquish(); }
   tc_fence_before();
@@ -1012,19 +1017,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     // Producer: K, V once; per Q tile, dO (released after dV^T) then Q
     // (released after dK^T), one barrier per 64-dim chunk.
     if (lane == 0) {
-      bool ok = true, any = false;
+      bool ok = true;
       int i = 0;
       uint32_t issued = 0;  // chunks issued for the current tile (bit c: q, bit HC+c: dO)
       for (int qt = qrng.x; qt < qrng.y && ok; ++qt) {
         if (tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN) == TILE_EMPTY) continue;
-        if (!any) {
-          any = true;
-          mbar_arrive_expect_tx(kv_full, 2 * HC * C::KV_CHUNK);
-          for (int c = 0; c < HC; ++c) {
-            tma_load_3d(sbase + C::k_off + c * C::KV_CHUNK, &a.tm_k, kv_full, c * 64, s0, bk);
-            tma_load_3d(sbase + C::v_off + c * C::KV_CHUNK, &a.tm_v, kv_full, c * 64, s0, bk);
-          }
-        }
         issued = 0;
         const int qb = i % QB;
         auto load_q = [&](int h) -> bool {
@@ -1235,6 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
     dkdv_epilogue<H, BN, SPLIT>(a, tmem + lane_base + C::dv_col, tmem + lane_base + C::dk_col, r, half,
                                 have, jt, split, bk, reinterpret_cast<volatile int*>(sm + C::misc_off + 16));
   }
+  if (tid == 0) mbar_wait_teardown(kv_full, 0, a.wait_limit_ns);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) { tc_fence_after(); tmem_dealloc(tmem, 512); }
