@@ -42,7 +42,19 @@ L2_BYTES = 129 * 2**20
 # by workload and kernel label (as kernel_names() gives it); valid only while
 # the kernel source's code (its comments aside) hashes to `src_sha`.  Each
 # entry names the capture it comes from in `note`.
-NCU_TRAFFIC: dict = {}
+_CAPTURE = ("one --metrics capture on one GB300 (medians of 15 launches; profiles/"
+            "launches_gqa_causal_h256_t8192.md); DRAM traffic of the same code varies "
+            "box to box with L2 residency")
+NCU_TRAFFIC: dict = {
+    "gqa_causal_h256_t8192": {
+        "fa_fwd_kernel<256>": {"bytes_per_launch": 108218000, "src": "fwd.cu",
+                               "src_sha": "d2b8009a8cd7663c", "note": _CAPTURE},
+        "fa_bwd_dkdv1_kernel<256, 64, 0>": {"bytes_per_launch": 193545000, "src": "bwd.cu",
+                                            "src_sha": "c3691a3bf755d84d", "note": _CAPTURE},
+        "fa_bwd_dq_kernel<256, 64>": {"bytes_per_launch": 188660000, "src": "bwd.cu",
+                                      "src_sha": "c3691a3bf755d84d", "note": _CAPTURE},
+    },
+}
 
 
 def kernel_names(w: inputs.Workload, n_splits: int, masked: bool) -> dict:
