@@ -329,7 +329,7 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   if (split_ok) {
     const int fs = g_bwd_q_splits.load();
     const bool uneven = causal || seg_q != nullptr || bm.cls != nullptr;
-    a.q_splits = fs != 0 ? fs : fa::bwd_q_splits(dkdv_ctas, sms, uneven);
+    a.q_splits = fs != 0 ? fs : fa::bwd_q_splits(dkdv_ctas, sms, uneven, H);
   }
   if (a.q_splits > 1) {
     a.dkv_count = counters;
@@ -520,7 +520,7 @@ int fa_bwd_plan(int B, int K, int G, int T, int S, int H, int causal, int masked
   const int kvr = fa::bwd_kv_rows(H, B, K, S, sm_count);
   const long ctas = (long)B * K * ((S + kvr - 1) / kvr);
   *kv_rows = kvr;
-  *q_splits = fa::bwd_q_splits(ctas, sm_count, causal != 0 || masked != 0);
+  *q_splits = fa::bwd_q_splits(ctas, sm_count, causal != 0 || masked != 0, H);
   return FA_OK;
 }
 

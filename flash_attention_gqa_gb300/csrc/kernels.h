@@ -96,15 +96,22 @@ inline int bwd_kv_rows(int H, int B, int K, int S, int sm_count) {
 constexpr int kMinBwdKvRows = 64;  // the workspace's range table is sized for it
 
 // Q-range split of the dK/dV grid.  With fewer dK/dV CTAs than SMs, the Q
-// tiles of each KV tile are dealt to q_splits CTAs.  The count in
-// 1..kMaxQSplits minimising waves / splits.  Ties go to the larger count when
-// the sweeps are uneven (causal, segment ids or a block mask: the first KV
-// tiles' sweeps are the longest, and splitting shortens them) and to the
-// smaller otherwise (equal sweeps: more CTAs only add waves and fixed costs).
-// 1 when the grid already fills the GPU.
+// tiles of each KV tile are dealt to q_splits CTAs (1..kMaxQSplits); 1 when the
+// grid already fills the GPU.  H <= 128: the largest count that keeps the grid
+// to one wave (a second wave of light CTAs, with their extra partial tiles to
+// write and add, measured slower than longer sweeps: T=1024 backward 53.4 us at
+// 4 splits, 46.8 us at 2).  H = 256, where a tile costs twice as much: the
+// count minimising waves / splits, ties going to the larger count when the
+// sweeps are uneven (causal, segment ids or a block mask: the first KV tiles'
+// sweeps are the longest) and to the smaller otherwise.
 constexpr int kMaxQSplits = 4;
-inline int bwd_q_splits(long ctas, int sm_count, bool uneven) {
+inline int bwd_q_splits(long ctas, int sm_count, bool uneven, int H) {
   if (ctas <= 0 || ctas >= sm_count) return 1;
+  if (H <= 128) {
+    int n = 1;
+    while (n < kMaxQSplits && ctas * (n + 1) <= sm_count) ++n;
+    return n;
+  }
   int best = 1;
   double best_cost = 1e30;
   for (int n = 1; n <= kMaxQSplits; ++n) {

@@ -251,9 +251,11 @@ int fa_set_bwd_kv_rows(int rows);
  * 0 (default) chooses per call, 1..4 forces that many CTAs per KV tile.  Either
  * applies only where the dK/dV grid is smaller than the GPU and the workspace
  * holds the split part (fa_bwd_workspace_size); elsewhere there is one CTA per
- * KV tile.  The default takes the count in 1..4 that minimises (waves of the
- * split grid) / count; ties go to the larger count for causal, segment-id or
- * block-masked calls (uneven sweeps) and to the smaller otherwise.  The result
+ * KV tile.  The default, for H <= 128, is the largest count in 1..4 that keeps
+ * the split grid to one wave; for H = 256, the count that minimises (waves of
+ * the split grid) / count, ties going to the larger count for causal,
+ * segment-id or block-masked calls (uneven sweeps) and to the smaller
+ * otherwise.  The result
  * does not depend on the choice beyond fp32 summation order.  Returns
  * FA_ERR_INVALID_ARG for any other value.
  */

@@ -160,11 +160,16 @@ def test_bwd_plan(clib):
     """The backward's grid plan on a 152-SM GPU (host logic, no device)."""
     plan = lambda *a: binding.fa_bwd_plan(*a)
     OK = binding.FA_OK
-    # T=1024 (B2 K2 G4 H128): 32 dK/dV CTAs at 128 keys -> 64-key tiles, 64 CTAs.
-    # waves/splits: 1, 1/2, 2/3, 2/4 -> causal ties to 4 splits, non-causal to 2
-    assert plan(2, 2, 4, 1024, 1024, 128, 1, 0, 152) == (OK, 64, 4)
+    # T=1024 (B2 K2 G4 H128): 32 dK/dV CTAs at 128 keys -> 64-key tiles, 64 CTAs;
+    # H <= 128 takes the largest split count that stays within one wave: 2 (128 CTAs)
+    assert plan(2, 2, 4, 1024, 1024, 128, 1, 0, 152) == (OK, 64, 2)
     assert plan(2, 2, 4, 1024, 1024, 128, 0, 0, 152) == (OK, 64, 2)
-    assert plan(2, 2, 4, 1024, 1024, 128, 0, 1, 152) == (OK, 64, 4)   # segments: uneven
+    assert plan(2, 2, 4, 1024, 1024, 128, 0, 1, 152) == (OK, 64, 2)
+    assert plan(1, 1, 4, 1024, 1024, 128, 1, 0, 152) == (OK, 64, 4)   # 16 CTAs: 4 fit
+    assert plan(1, 5, 4, 2048, 2048, 128, 1, 0, 152) == (OK, 64, 1)   # 160 CTAs: full
+    # H=256 T=2048 (B1 K2): 64 CTAs of 64 keys; waves/splits 1, 1/2, 2/3, 2/4 -> causal ties to 4
+    assert plan(1, 2, 8, 2048, 2048, 256, 1, 0, 152) == (OK, 64, 4)
+    assert plan(1, 2, 8, 2048, 2048, 256, 0, 0, 152) == (OK, 64, 2)
     # H=256 T=8192 (B1 K2): 256 CTAs of 64 keys fill the GPU
     assert plan(1, 2, 8, 8192, 8192, 256, 1, 0, 152) == (OK, 64, 1)
     # packed documents (B4 K8 H128 T=4096): 1024 CTAs of 128 keys
@@ -175,7 +180,7 @@ def test_bwd_plan(clib):
     # no SMs reported: nothing is split, H=128 keeps 128-key tiles
     assert plan(1, 1, 4, 128, 128, 128, 1, 0, 0) == (OK, 128, 1)
     # H = 64 follows the H = 128 rule (it runs the H = 128 kernels)
-    assert plan(2, 2, 4, 1024, 1024, 64, 1, 0, 152) == (OK, 64, 4)
+    assert plan(2, 2, 4, 1024, 1024, 64, 1, 0, 152) == (OK, 64, 2)
     assert plan(4, 8, 4, 4096, 4096, 64, 1, 1, 152) == (OK, 128, 1)
     assert plan(1, 1, 4, 128, 128, 96, 1, 0, 152)[0] == binding.FA_ERR_UNSUPPORTED
     assert plan(1, 1, 4, 128, 128, 128, 1, 0, -1)[0] == binding.FA_ERR_INVALID_ARG
