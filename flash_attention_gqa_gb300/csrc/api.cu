@@ -313,6 +313,7 @@ int bwd_impl(int stage, const void* q, const void* k, const void* v, const void*
   a.lse = lse;
   a.delta = delta;
   a.seg_ranges = ranges;
+  a.seg_runs = reinterpret_cast<uint8_t*>(static_cast<char*>(workspace) + wl.runs);
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.seg_q = seg_q; a.seg_kv = seg_kv;
   a.B = B; a.K = K; a.G = G; a.T = T; a.S = S; a.H = H;
@@ -462,7 +463,7 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    void* stream) {
   const int rc = check_shapes(B, K, G, T, S, H, causal, seg_q, seg_kv);
   if (rc != FA_OK) return rc;
-  // Only the base part (D rows, range table) lives in the scratch: no Q-range split here.
+  // Only the base part (D rows, segment tables) lives in the scratch: no Q-range split here.
   if (fa::bwd_workspace(B, K, G, T, S, H, 0).base > (size_t)FA_NOALLOC_SCRATCH_BYTES)
     return FA_ERR_UNSUPPORTED;
   void* scratch = noalloc_scratch_address();

@@ -87,33 +87,71 @@ __device__ __forceinline__ int causal_kv_end(const BwdArgs& a, int t0, int Tb, i
   return lim < 0 ? 0 : min(a.n_kvtiles, lim / kvr + 1);
 }
 
-// Apply the causal / segment / key-range mask to 32 consecutive key columns
-// [scol, scol + 32) of the row at position t.
-__device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int kh, int g, int t,
-                                       int my_seg, int scol) {
-  const int off = a.S - a.T;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int sc = scol + i;
-    if (sc >= a.S || (a.causal && sc > t + off)) s[i] = -INFINITY;
-  }
+// The keys of a KV tile that a query row keeps, as far as the causal limit,
+// the end of the keys and (for tiles whose segment ids form at most two runs)
+// the row's segment id decide them: [klo, khi) relative to the tile's first
+// key s0.  per_key: the tile's ids form more runs; mask32 then compares them
+// one by one.
+struct RowKeep {
+  int klo, khi;
+  bool per_key;
+};
+__device__ __forceinline__ RowKeep row_keep(const BwdArgs& a, int b, int jt, int s0, int t, int my_seg) {
+  const int n_keys = min(a.kv_rows, a.S - s0);
+  RowKeep k{0, n_keys, false};
+  if (a.causal) k.khi = min(k.khi, t + (a.S - a.T) - s0 + 1);
   if (a.seg_q != nullptr) {
-    const int32_t* ids = a.seg_kv + (long)b * a.S + scol;
-    if ((a.S & 3) == 0 && scol + 32 <= a.S) {  // 16-byte aligned, in range: vector loads
-      const int4* kid = reinterpret_cast<const int4*>(ids);
-#pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const int4 v = __ldg(kid + i4);
-        if (v.x != my_seg) s[4 * i4 + 0] = -INFINITY;
-        if (v.y != my_seg) s[4 * i4 + 1] = -INFINITY;
-        if (v.z != my_seg) s[4 * i4 + 2] = -INFINITY;
-        if (v.w != my_seg) s[4 * i4 + 3] = -INFINITY;
-      }
+    const int runs = a.seg_runs[(long)b * a.n_kvtiles + jt];
+    if (runs == kRunsGeneral) {
+      k.per_key = true;
     } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (scol + i < a.S && __ldg(ids + i) != my_seg) s[i] = -INFINITY;
+      const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
+      if (my_seg == __ldg(ids)) k.khi = min(k.khi, runs);
+      else if (runs < n_keys && my_seg == __ldg(ids + n_keys - 1)) k.klo = runs;
+      else k.khi = 0;
     }
+  }
+  return k;
+}
+
+// Apply the mask to 32 consecutive key columns [scol, scol + 32) of the row at
+// position t.  SEGS (segment ids given): `keep` is the row's row_keep for the
+// tile starting at s0.  Without segment ids only the causal limit and the end
+// of the keys apply, as one range of kept columns (and the block mask, as in
+// both cases); those kernels carry no segment code at all.
+template <bool SEGS>
+__device__ __forceinline__ void mask32(float (&s)[32], const BwdArgs& a, int b, int kh, int g, int t,
+                                       int my_seg, int scol, int s0, const RowKeep& keep) {
+  if constexpr (SEGS) {
+    const uint32_t kept = range_bits(keep.klo - (scol - s0), keep.khi - (scol - s0));
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!((kept >> i) & 1u)) s[i] = -INFINITY;
+    if (keep.per_key) {
+      const int32_t* ids = a.seg_kv + (long)b * a.S + scol;
+      if ((a.S & 3) == 0 && scol + 32 <= a.S) {  // 16-byte aligned, in range: vector loads
+        const int4* kid = reinterpret_cast<const int4*>(ids);
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int4 v = __ldg(kid + i4);
+          if (v.x != my_seg) s[4 * i4 + 0] = -INFINITY;
+          if (v.y != my_seg) s[4 * i4 + 1] = -INFINITY;
+          if (v.z != my_seg) s[4 * i4 + 2] = -INFINITY;
+          if (v.w != my_seg) s[4 * i4 + 3] = -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (scol + i < a.S && __ldg(ids + i) != my_seg) s[i] = -INFINITY;
+      }
+    }
+  } else {
+    int khi = a.S - scol;
+    if (a.causal) khi = min(khi, t + (a.S - a.T) - scol + 1);
+    const uint32_t kept = range_bits(0, khi);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!((kept >> i) & 1u)) s[i] = -INFINITY;
   }
   if (a.bm.cls != nullptr && t < a.T) {
     const uint32_t bits = bm_row_word(a.bm, kh, a.G, g, t, scol >> 7, (scol & 127) >> 5);
@@ -199,7 +237,7 @@ struct DqCfg {
   __host__ __device__ static constexpr uint32_t dp_col(int u) { return H + NBS * BN + u * BN; }
 };
 
-template <int H, int BN_>
+template <int H, int BN_, bool SEGS>
 __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<H, BN_>;
   constexpr int HC = C::HC, BN = C::BN, NBS = C::NBS, NBP = C::NBP, KSL = C::KSL, VSL = C::VSL;
@@ -448,6 +486,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
       const int cls = tile_class(a, qr, kr, b, bk % a.K, qt, jt, Tb, BN);
       if (cls == TILE_EMPTY) continue;
       const int us = n % NBS, up = n % NBP;
+      RowKeep keep{};
+      if constexpr (SEGS)
+        if (cls == TILE_PARTIAL) keep = row_keep(a, b, jt, jt * BN, t, my_seg);
       if (!warp_wait(sdp_full(n & 1), (n >> 1) & 1, ab)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
@@ -457,7 +498,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) fa_bwd_dq_kernel(const __grid_c
         tmem_ld32(tmem + lane_base + C::dp_col(up) + c * 32, pv);
         tmem_wait_ld();
         float* s = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, jt * BN + c * 32);
+        if (cls == TILE_PARTIAL)
+          mask32<SEGS>(*reinterpret_cast<float(*)[32]>(s), a, b, bk % a.K, g, t, my_seg, jt * BN + c * 32,
+                       jt * BN, keep);
         uint32_t ds[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -671,7 +714,7 @@ struct Dkv1Cfg {
   static constexpr uint32_t dp_col = 2 * HH * BN + BN;
 };
 
-template <int H, int BN_, bool SPLIT>
+template <int H, int BN_, bool SPLIT, bool SEGS>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_constant__ BwdArgs a) {
   using C = Dkv1Cfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN;
@@ -849,6 +892,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
       const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
       const float Dr = valid ? a.delta[row] : 0.f;
       const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
+      RowKeep keep{};
+      if constexpr (SEGS)
+        if (cls == TILE_PARTIAL) keep = row_keep(a, b, jt, s0, t, my_seg);
       // Phase 1: P = exp(S - lse) once S(i) is done.  s_full is A's commit, which
       // also covers dK^T(i-1) (the reader of the dS buffer); the P buffer's
       // reader dV^T(i-1) is B's, so its release barrier is waited for here.
@@ -863,7 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv1_kernel(const __grid_
         tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
         tmem_wait_ld();
         float* sf = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
+        if (cls == TILE_PARTIAL)
+          mask32<SEGS>(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32, s0, keep);
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           pp[cc][k] = pack_bf16x2(fast_exp2(fmaf(sf[2 * k], kLog2e, -lse2)),
@@ -942,7 +989,7 @@ struct DkvCfg {
   static constexpr uint32_t dp_col = 2 * HH * BN + BN;
 };
 
-template <int H, int BN_, bool SPLIT>
+template <int H, int BN_, bool SPLIT, bool SEGS>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkvCfg<H, BN_>;
   constexpr int HC = C::HC, HH = C::HH, BN = C::BN, QB = C::QB;
@@ -1170,6 +1217,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
       const float lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
       const float Dr = valid ? a.delta[row] : 0.f;
       const int my_seg = (a.seg_q && valid) ? a.seg_q[(long)b * a.T + t] : 0;
+      RowKeep keep{};
+      if constexpr (SEGS)
+        if (cls == TILE_PARTIAL) keep = row_keep(a, b, jt, s0, t, my_seg);
       // Phase 1: P = exp(S - lse) once S(i) is done, computed into registers
       // first; the P buffer is then overwritten once its reader dV^T(i-1)
       // (issuer B's) is done.
@@ -1183,7 +1233,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_dkdv_kernel(const __grid_c
         tmem_ld32(tmem + lane_base + C::s_col + c * 32, sv);
         tmem_wait_ld();
         float* sf = reinterpret_cast<float*>(sv);
-        if (cls == TILE_PARTIAL) mask32(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32);
+        if (cls == TILE_PARTIAL)
+          mask32<SEGS>(*reinterpret_cast<float(*)[32]>(sf), a, b, bk % a.K, g, t, my_seg, s0 + c * 32, s0, keep);
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           pp[cc][k] = pack_bf16x2(fast_exp2(fmaf(sf[2 * k], kLog2e, -lse2)),
@@ -1285,9 +1336,10 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
   }
 }
 
-// Per-tile [min, max] of segment ids: one warp per (b, tile).
+// Per-tile [min, max] of segment ids: one warp per (b, tile).  With `runs`
+// (the KV tiles), also each tile's segment-run byte (see kRunsGeneral).
 __global__ void seg_ranges_kernel(const int32_t* __restrict__ seg, int L, int tile, int n_tiles,
-                                  long total, int2* __restrict__ out) {
+                                  long total, int2* __restrict__ out, uint8_t* __restrict__ runs) {
   const long w = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (w >= total) return;
@@ -1296,14 +1348,26 @@ __global__ void seg_ranges_kernel(const int32_t* __restrict__ seg, int L, int ti
   const int32_t* p = seg + b * L + (long)j * tile;
   const int n = min(tile, L - j * tile);  // the last tile may be ragged
   int mn = INT_MAX, mx = INT_MIN;
-  for (int i = lane; i < n; i += 32) {
-    const int v = __ldg(p + i);
+  int changes = 0, pos = tile, prev_last = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {  // uniform over the warp
+    const int i = i0 + lane;
+    const int v = __ldg(p + min(i, n - 1));  // past the end: the last id again
     mn = min(mn, v);
     mx = max(mx, v);
+    const int left = __shfl_up_sync(0xffffffffu, v, 1);
+    const bool change = i > 0 && i < n && v != (lane == 0 ? prev_last : left);
+    const uint32_t m = __ballot_sync(0xffffffffu, change);
+    if (m != 0u && changes == 0) pos = i0 + __ffs((int)m) - 1;  // first key of the second run
+    changes += __popc(m);
+    prev_last = __shfl_sync(0xffffffffu, v, 31);
   }
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) out[w] = make_int2(mn, mx);
+  if (lane == 0) {
+    out[w] = make_int2(mn, mx);
+    if (runs != nullptr)
+      runs[w] = changes == 0 ? (uint8_t)tile : changes == 1 ? (uint8_t)pos : kRunsGeneral;
+  }
 }
 
 template <typename Kern>
@@ -1316,10 +1380,10 @@ cudaError_t set_smem(Kern k, uint32_t bytes, int* configured) {
   return e;
 }
 
-template <int H, int BN>
+template <int H, int BN, bool SEGS>
 cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dq_kernel<H, BN>, DqCfg<H, BN>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dq_kernel<H, BN, SEGS>, DqCfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_qtiles * a.B * a.K);
@@ -1331,27 +1395,40 @@ cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H, BN>, a);
+  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<H, BN, SEGS>, a);
+}
+template <int H, int BN>
+cudaError_t launch_dq_h(const BwdArgs& a, cudaStream_t st, bool overlap_previous) {
+  return a.seg_q != nullptr ? launch_dq_h<H, BN, true>(a, st, overlap_previous)
+                            : launch_dq_h<H, BN, false>(a, st, overlap_previous);
 }
 
-template <int H, int BN, bool SPLIT>
+template <int H, int BN, bool SPLIT, bool SEGS>
 cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H, BN, SPLIT>, DkvCfg<H, BN>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dkdv_kernel<H, BN, SPLIT, SEGS>, DkvCfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<H, BN, SPLIT><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K), kThreads,
-                                     DkvCfg<H, BN>::alloc, st>>>(a);
+  fa_bwd_dkdv_kernel<H, BN, SPLIT, SEGS><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K),
+                                           kThreads, DkvCfg<H, BN>::alloc, st>>>(a);
   return cudaGetLastError();
 }
-
 template <int H, int BN, bool SPLIT>
+cudaError_t launch_dkdv_h(const BwdArgs& a, cudaStream_t st) {
+  return a.seg_q != nullptr ? launch_dkdv_h<H, BN, SPLIT, true>(a, st) : launch_dkdv_h<H, BN, SPLIT, false>(a, st);
+}
+
+template <int H, int BN, bool SPLIT, bool SEGS>
 cudaError_t launch_dkdv1_h(const BwdArgs& a, cudaStream_t st) {
   static int configured = -1;
-  cudaError_t e = set_smem(fa_bwd_dkdv1_kernel<H, BN, SPLIT>, Dkv1Cfg<H, BN>::alloc, &configured);
+  cudaError_t e = set_smem(fa_bwd_dkdv1_kernel<H, BN, SPLIT, SEGS>, Dkv1Cfg<H, BN>::alloc, &configured);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv1_kernel<H, BN, SPLIT><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K), kThreads,
-                                      Dkv1Cfg<H, BN>::alloc, st>>>(a);
+  fa_bwd_dkdv1_kernel<H, BN, SPLIT, SEGS><<<dim3(a.n_kvtiles * (SPLIT ? a.q_splits : 1) * a.B * a.K),
+                                            kThreads, Dkv1Cfg<H, BN>::alloc, st>>>(a);
   return cudaGetLastError();
+}
+template <int H, int BN, bool SPLIT>
+cudaError_t launch_dkdv1_h(const BwdArgs& a, cudaStream_t st) {
+  return a.seg_q != nullptr ? launch_dkdv1_h<H, BN, SPLIT, true>(a, st) : launch_dkdv1_h<H, BN, SPLIT, false>(a, st);
 }
 
 }  // namespace
@@ -1362,7 +1439,8 @@ BwdWorkspace bwd_workspace(int B, int K, int G, int T, int S, int H, int sm_coun
   const size_t tb = kRows / G, kvr = kMinBwdKvRows;
   const size_t nq = (T + tb - 1) / tb, nk = (S + kvr - 1) / kvr;
   const size_t r = up((size_t)B * (nq + nk) * sizeof(int2));
-  BwdWorkspace w{d, 0, 0, d + r, d + r};
+  const size_t ru = up((size_t)B * nk);  // one segment-run byte per KV tile
+  BwdWorkspace w{d, d + r, 0, 0, d + r + ru, d + r + ru};
   // Every KV tile size the backward may pick for H: the largest split part.
   size_t cnt = 0, part = 0;
   const size_t Hk = H < 128 ? 128 : H;  // the kernels' head dim (H = 64 runs as 128)
@@ -1407,9 +1485,9 @@ cudaError_t launch_seg_ranges(const BwdArgs& a, cudaStream_t st) {
   const long nq = (long)a.B * a.n_qtiles, nk = (long)a.B * a.n_kvtiles;
   const int warps = 8;
   seg_ranges_kernel<<<(unsigned)((nq + warps - 1) / warps), warps * 32, 0, st>>>(a.seg_q, a.T, Tb,
-                                                                                a.n_qtiles, nq, qr);
+                                                                                a.n_qtiles, nq, qr, nullptr);
   seg_ranges_kernel<<<(unsigned)((nk + warps - 1) / warps), warps * 32, 0, st>>>(
-      a.seg_kv, a.S, a.kv_rows, a.n_kvtiles, nk, kr);
+      a.seg_kv, a.S, a.kv_rows, a.n_kvtiles, nk, kr, a.seg_runs);
   return cudaGetLastError();
 }
 

@@ -42,7 +42,8 @@ struct FwdSmem {
   static constexpr uint32_t ring_off = HC * kChunkBytes;
   static constexpr uint32_t tiles_off = ring_off + kSlots * kChunkBytes;   // uint16 schedule
   static constexpr uint32_t cls_off = tiles_off + kMaxKvTiles * 2;         // uint8 classes
-  static constexpr uint32_t bar_off = cls_off + kMaxKvTiles;
+  static constexpr uint32_t runs_off = cls_off + kMaxKvTiles;               // uint8 segment runs
+  static constexpr uint32_t bar_off = runs_off + kMaxKvTiles;
   // barriers: q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], pv_done[2], teardown
   static constexpr int n_bars = 1 + 2 * kSlots + 7;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, count, qrange
@@ -88,8 +89,8 @@ enum : uint8_t { TILE_EMPTY = 0, TILE_FULL = 1, TILE_PARTIAL = 2 };
 // [o_col, o_col + H).  Returns false when a bounded wait gave up.
 template <int H>
 __device__ __forceinline__ bool softmax_tile(const FwdArgs& a, uint32_t tmem, uint32_t lane_base,
-                                             uint16_t entry, int n, int N, int t, int g, bool valid,
-                                             int my_seg, int b, int kh, const Bars& bars,
+                                             uint16_t entry, uint8_t runs, int n, int N, int t, int g,
+                                             bool valid, int my_seg, int b, int kh, const Bars& bars,
                                              const Abort& ab, float& m_ref, float& l,
                                              uint32_t o_col = 0) {
   const int j = entry & 0x7fff;
@@ -105,12 +106,33 @@ __device__ __forceinline__ bool softmax_tile(const FwdArgs& a, uint32_t tmem, ui
   tmem_wait_ld();
   float* s = reinterpret_cast<float*>(&sv[0][0]);
   if (partial) {
+    // Keys kept by the causal and range limits form [klo, khi); with segment
+    // ids in at most two runs (`runs` < kRunsGeneral) the row's id selects one
+    // run, which narrows the same range.  The range becomes four 32-bit keep
+    // words, one select per score.  Other segment layouts compare ids one by one.
     const int s0 = j * kKvRows;
-    const int lim = a.causal ? min(t + off, a.S - 1) : a.S - 1;  // last key kept
-#pragma unroll
-    for (int c = 0; c < 128; ++c)
-      if (s0 + c > lim) s[c] = -INFINITY;
+    const int n_keys = min(kKvRows, a.S - s0);
+    int klo = 0, khi = n_keys;
+    if (a.causal) khi = min(khi, t + off - s0 + 1);
+    bool per_key = false;
     if (segs) {
+      if (runs != kRunsGeneral) {
+        const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
+        if (my_seg == __ldg(ids)) khi = min(khi, (int)runs);
+        else if (runs < n_keys && my_seg == __ldg(ids + n_keys - 1)) klo = runs;
+        else khi = 0;
+      } else {
+        per_key = true;
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t keep = range_bits(klo - 32 * w, khi - 32 * w);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (!((keep >> i) & 1u)) s[32 * w + i] = -INFINITY;
+    }
+    if (per_key) {
       // every thread reads the same 512 B of key ids: served by L1 broadcast
       const int32_t* ids = a.seg_kv + (long)b * a.S + s0;
       if ((a.S & 3) == 0 && s0 + 128 <= a.S) {  // aligned and in range
@@ -236,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 
   uint16_t* tiles = reinterpret_cast<uint16_t*>(sm + L::tiles_off);
   uint8_t* cls = sm + L::cls_off;
+  uint8_t* runs = sm + L::runs_off;  // per KV tile j (segment ids only)
   Bars bars{sbase + L::bar_off};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc_off + 4);
@@ -318,20 +341,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (a.causal && s_last > t0 + off) c = TILE_PARTIAL;  // crosses the diagonal
     if ((j + 1) * kKvRows > a.S) c = TILE_PARTIAL;         // ragged last tile
     if (segs) {
-      int mn = INT_MAX, mx = INT_MIN;
+      // 4 keys per lane; keys past S repeat the last key's id (no effect on the
+      // range, no extra run)
+      int mn = INT_MAX, mx = INT_MIN, v[4];
       for (int e = 0; e < 4; ++e) {
-        const int sk = j * kKvRows + lane * 4 + e;
-        if (sk < a.S) {
-          const int v = a.seg_kv[(long)b * a.S + sk];
-          mn = min(mn, v);
-          mx = max(mx, v);
-        }
+        v[e] = a.seg_kv[(long)b * a.S + min(j * kKvRows + lane * 4 + e, s_last)];
+        mn = min(mn, v[e]);
+        mx = max(mx, v[e]);
       }
       mn = __reduce_min_sync(0xffffffffu, mn);
       mx = __reduce_max_sync(0xffffffffu, mx);
       const int qmn = qrange[0], qmx = qrange[1];
       if (mx < qmn || mn > qmx) c = TILE_EMPTY;
       else if (!(mn == mx && qmn == qmx && mn == qmn)) c = TILE_PARTIAL;
+      // where the id changes, if it changes at most once
+      int changes = (v[1] != v[0]) + (v[2] != v[1]) + (v[3] != v[2]);
+      int pos = v[1] != v[0] ? 4 * lane + 1 : v[2] != v[1] ? 4 * lane + 2 : v[3] != v[2] ? 4 * lane + 3 : kKvRows;
+      const int prev = __shfl_up_sync(0xffffffffu, v[3], 1);
+      if (lane > 0 && v[0] != prev) { ++changes; pos = 4 * lane; }
+      changes = __reduce_add_sync(0xffffffffu, changes);
+      pos = __reduce_min_sync(0xffffffffu, pos);
+      if (lane == 0) runs[j] = changes == 0 ? (uint8_t)kKvRows : changes == 1 ? (uint8_t)pos : kRunsGeneral;
     }
     if (a.bm.cls != nullptr)  // the Q tile lies inside one 128-position mask block
       c = (uint8_t)class_and(c, bm_tile_class(a.bm, bk % a.K, a.G, t0 >> 7, j));
@@ -465,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     float l = 0.f;            // running denominator (relative to m_ref)
     bool ok = true;
     for (int n = 0; n < n_tiles; ++n) {
-      if (!softmax_tile<H>(a, tmem, lane_base, sched[n], n, n, t, g, valid, my_seg, b, bk % a.K,
+      if (!softmax_tile<H>(a, tmem, lane_base, sched[n], segs ? runs[sched[n] & 0x7fff] : kRunsGeneral,
+                           n, n, t, g, valid, my_seg, b, bk % a.K,
                            bars, ab, m_ref, l)) {
         ok = false;
         break;
@@ -551,7 +582,8 @@ struct PFwdSmem {
   static constexpr uint32_t q_off = 0;  // Q[b] at q_off + b * HC * kChunkBytes
   static constexpr uint32_t ring_off = 2 * HC * kChunkBytes;
   static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[2][kMaxKvTiles]
-  static constexpr uint32_t bar_off = sched_off + 2 * kMaxKvTiles * 2;
+  static constexpr uint32_t runs_off = sched_off + 2 * kMaxKvTiles * 2;   // uint8[2][kMaxKvTiles]
+  static constexpr uint32_t bar_off = runs_off + 2 * kMaxKvTiles;
   // q_full[2], sched_full[2], item_free[2], then the Bars block (full, empty,
   // s_full, p_full, pv_done, teardown), the O += P V issuer's teardown, and
   // o_staged
@@ -581,6 +613,8 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
   // before reaching it)
   const uint32_t o_staged = pb + 8 * (6 + 1 + 2 * kSlots + 7 + 1);
   auto sched = [&](int b) { return reinterpret_cast<uint16_t*>(sm + L::sched_off) + b * kMaxKvTiles; };
+  // segment-run byte of each schedule entry (segment ids only)
+  auto runs_of = [&](int b) { return sm + L::runs_off + b * kMaxKvTiles; };
   auto q_tile = [&](int b) { return L::q_off + (uint32_t)b * HC * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc_off + 4);
@@ -666,7 +700,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       int count = 0;
       for (int j0 = 0; j0 < n_kv; j0 += 32) {
         const int j = j0 + lane;
-        uint8_t c = TILE_EMPTY;
+        uint8_t c = TILE_EMPTY, run = kRunsGeneral;
         if (j < n_kv) {
           c = TILE_FULL;
           const int s_first = j * kKvRows, s_last = min(s_first + kKvRows, a.S) - 1;
@@ -674,6 +708,8 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           if (s_first + kKvRows > a.S) c = TILE_PARTIAL;         // ragged last tile
           if (segs) {
             int mn = INT_MAX, mx = INT_MIN;
+            // where the id changes, if it changes at most once
+            int prev = 0, changes = 0, pos = kKvRows;
             const int32_t* ids = a.seg_kv + (long)bb * a.S + s_first;
             if ((a.S & 3) == 0 && s_first + kKvRows <= a.S) {
               const int4* kid = reinterpret_cast<const int4*>(ids);
@@ -682,23 +718,34 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
                 const int4 v = __ldg(kid + e);
                 mn = min(min(mn, v.x), min(v.y, min(v.z, v.w)));
                 mx = max(max(mx, v.x), max(v.y, max(v.z, v.w)));
+                if (e > 0 && v.x != prev && changes++ == 0) pos = 4 * e;
+                if (v.y != v.x && changes++ == 0) pos = 4 * e + 1;
+                if (v.z != v.y && changes++ == 0) pos = 4 * e + 2;
+                if (v.w != v.z && changes++ == 0) pos = 4 * e + 3;
+                prev = v.w;
               }
             } else {
               for (int e = 0; e <= s_last - s_first; ++e) {
                 const int v = __ldg(ids + e);
                 mn = min(mn, v);
                 mx = max(mx, v);
+                if (e > 0 && v != prev && changes++ == 0) pos = e;
+                prev = v;
               }
             }
             if (mx < qmn || mn > qmx) c = TILE_EMPTY;
             else if (!(mn == mx && qmn == qmx && mn == qmn)) c = TILE_PARTIAL;
+            run = changes == 0 ? (uint8_t)kKvRows : changes == 1 ? (uint8_t)pos : kRunsGeneral;
           }
           if (c != TILE_EMPTY && a.bm.cls != nullptr)  // the Q tile lies inside one 128-position block
             c = (uint8_t)class_and(c, bm_tile_class(a.bm, bk % a.K, a.G, t0 >> 7, j));
         }
         const uint32_t m = __ballot_sync(0xffffffffu, c != TILE_EMPTY);
-        if (c != TILE_EMPTY)
-          list[count + __popc(m & ((1u << lane) - 1))] = (uint16_t)(j | (c == TILE_PARTIAL ? 0x8000 : 0));
+        if (c != TILE_EMPTY) {
+          const int at = count + __popc(m & ((1u << lane) - 1));
+          list[at] = (uint16_t)(j | (c == TILE_PARTIAL ? 0x8000 : 0));
+          runs_of(b)[at] = run;
+        }
         count += __popc(m);
       }
       __syncwarp();
@@ -871,7 +918,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       const uint32_t o_col = 128u * b;
       float m_ref = -INFINITY, l = 0.f;
       for (int n = 0; n < n_tiles; ++n) {
-        if (!softmax_tile<H>(a, tmem, lane_base, list[n], n, N + n, t, g, valid, my_seg, bb,
+        if (!softmax_tile<H>(a, tmem, lane_base, list[n], runs_of(b)[n], n, N + n, t, g, valid, my_seg, bb,
                              bk % a.K, bars, ab, m_ref, l, o_col)) {
           ok = false;
           break;

@@ -11,6 +11,12 @@ constexpr int kRows = 128;     // packed query rows per Q tile (G heads x 128/G 
 constexpr int kKvRows = 128;   // key/value rows per KV tile in the forward
 constexpr int kMaxKvTiles = 1024;  // S <= 131072
 
+// Segment-id layout of a KV tile, one byte per tile: the index of the key
+// where the id changes when the tile's ids form at most two runs (the tile's
+// key count when they form one), else kRunsGeneral.  Where it is not
+// kRunsGeneral, the keys a query row keeps are one contiguous range.
+constexpr uint8_t kRunsGeneral = 0xff;
+
 // Block-sparse mask metadata (device pointers; cls == nullptr: no mask).
 struct BlockMask {
   const uint8_t* cls;     // [heads, nqb, nkb] EMPTY / FULL / PARTIAL
@@ -51,6 +57,8 @@ struct BwdArgs {
   // Per-tile [min, max] segment ids (read only with segment ids): B * n_qtiles
   // Q-tile pairs, then B * n_kvtiles KV-tile pairs.  8-byte aligned.
   int2* seg_ranges;
+  // Segment-run byte of each KV tile (see kRunsGeneral): B * n_kvtiles bytes.
+  uint8_t* seg_runs;
   void* dq;            // bf16 [B*K, G, T, H]
   void* dk;            // bf16 [B*K, S, H]
   void* dv;            // bf16 [B*K, S, H]
@@ -127,6 +135,7 @@ inline int bwd_q_splits(long ctas, int sm_count, bool uneven, int H) {
 // partial dK/dV tiles per dK/dV CTA.
 struct BwdWorkspace {
   size_t ranges;    // offset of the segment-range table (256-byte aligned)
+  size_t runs;      // offset of the KV tiles' segment-run bytes (256-byte aligned)
   size_t counters;  // offset of the split counters (0 where no split can apply)
   size_t partials;  // offset of the partial tiles
   size_t base;      // bytes without the split part

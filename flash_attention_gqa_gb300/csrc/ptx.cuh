@@ -312,6 +312,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
          ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Bits [lo, hi) of a 32-bit word, the bounds clamped to [0, 32].
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > 32 ? 32 : hi;
+  if (hi <= lo) return 0u;
+  const uint32_t upto_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  const uint32_t upto_lo = (1u << lo) - 1u;  // lo < hi <= 32, so lo < 32
+  return upto_hi & ~upto_lo;
+}
+
 // ------------------------------------------------------------ conversions
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

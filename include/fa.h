@@ -140,8 +140,8 @@ int fa_block_mask_build(const uint8_t* dense, int heads, int T, int S,
    0 for empty or unsupported sizes), on the current device.  Where the dK/dV
    grid (one CTA per KV tile and b*K) is smaller than the GPU, the size
    includes the split part: kernel counters and fp32 partial dK/dV tiles for up
-   to 4 CTAs per KV tile.  fa_bwd runs with less, down to the D rows and range
-   table, but then without the Q-range split. */
+   to 4 CTAs per KV tile.  fa_bwd runs with less, down to the D rows and the
+   per-tile segment tables, but then without the Q-range split. */
 size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
 
 /*
@@ -152,8 +152,9 @@ size_t fa_bwd_workspace_size(int B, int K, int G, int T, int S, int H);
  * The pages give no backward; this is the textbook derivative of the forward
  * definition above.  `o` and `lse` must be those fa_fwd produced for the same
  * inputs.  `workspace` (>= fa_bwd_workspace_size bytes, 256-byte aligned)
- * holds the fp32 D rows and per-tile segment-id ranges and, for small grids,
- * the split part; its contents on entry do not matter.
+ * holds the fp32 D rows, the per-tile segment-id ranges, one byte per KV
+ * tile locating where its segment id changes (when it changes at most once)
+ * and, for small grids, the split part; its contents on entry do not matter.
  * Where the dK/dV grid is smaller than the GPU, the Q tiles of each KV tile are
  * dealt to up to 4 CTAs (fa_set_bwd_q_splits).  Each stores fp32 partial dK,
  * dV.  The last of them to finish adds the partials in a fixed order, so the
@@ -172,7 +173,7 @@ int fa_bwd(const void* q, const void* k, const void* v,
 
 /*
  * One stage of fa_bwd, with the same arguments: stage 0 computes D and the
- * per-tile segment ranges into the workspace, stage 1 writes dk and dv,
+ * per-tile segment tables into the workspace, stage 1 writes dk and dv,
  * stage 2 writes dq.  fa_bwd runs 0, 1, 2 in that order on `stream`; stages 1
  * and 2 read only the inputs and stage 0's workspace, so a caller may run
  * them on two streams once stage 0 is done.  Returns FA_ERR_INVALID_ARG for
@@ -200,11 +201,11 @@ int fa_bwd_stage(int stage, const void* q, const void* k, const void* v,
  * order); with that split forced off in fa_bwd (fa_set_bwd_q_splits(1)) the
  * two give the same bits.  The pages have no counterpart to this call.
  *
- * The scratch (fp32 D rows plus per-tile segment ranges, the same data fa_bwd
+ * The scratch (fp32 D rows plus per-tile segment tables, the same data fa_bwd
  * keeps in its workspace) is one fixed array of FA_NOALLOC_SCRATCH_BYTES in
  * the library's device memory, present on every GPU that loads the library
  * until the process exits.  Sizes whose scratch would not fit
- * (D rows and range table over FA_NOALLOC_SCRATCH_BYTES, i.e. roughly
+ * (D rows and tile tables over FA_NOALLOC_SCRATCH_BYTES, i.e. roughly
  * B*K*G*T > 2 million query rows) are rejected with FA_ERR_UNSUPPORTED before
  * anything is enqueued.
  *

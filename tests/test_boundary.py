@@ -58,20 +58,22 @@ def _split_part(B, K, S, H, sms):
 
 def test_workspace_size(clib):
     sms = binding.load().fa_device_sm_count()   # 0 without a GPU: no split part
-    # fp32 D rows, then one (min, max) int32 pair per (b, q tile) and (b, kv tile)
+    # fp32 D rows, then one (min, max) int32 pair per (b, q tile) and (b, kv tile),
+    # then one segment-run byte per (b, kv tile), each part rounded up to 256 B
     n = binding.fa_bwd_workspace_size(1, 2, 8, 8192, 8192, 256)
-    assert n == 2 * 8 * 8192 * 4 + (8192 // 16 + 8192 // 64) * 8 + _split_part(1, 2, 8192, 256, sms)
+    assert n == 2 * 8 * 8192 * 4 + (8192 // 16 + 8192 // 64) * 8 + 256 + \
+        _split_part(1, 2, 8192, 256, sms)
     assert n % 256 == 0
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256 + \
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 128, 128, 128) == 512 + 256 + 256 + \
         _split_part(1, 1, 128, 128, sms)
     assert binding.fa_bwd_workspace_size(0, 1, 1, 128, 128, 128) == 0
     # ragged sizes: D rows rounded up to 256 B, then one range pair per tile
-    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256 + \
+    assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 130, 128) == 512 + 256 + 256 + \
         _split_part(1, 1, 130, 128, sms)
     assert binding.fa_bwd_workspace_size(1, 1, 1, 100, 128, 96) == 0      # H unsupported
     # H = 64: D rows and range table as for any H, the split part at 128 head dims
     assert binding.fa_bwd_workspace_size(2, 2, 4, 1024, 1024, 64) == 2 * 2 * 4 * 1024 * 4 + \
-        256 * ((2 * (1024 // 32 + 1024 // 64) * 8 + 255) // 256) + _split_part(2, 2, 1024, 64, sms)
+        256 * ((2 * (1024 // 32 + 1024 // 64) * 8 + 255) // 256) + 256 + _split_part(2, 2, 1024, 64, sms)
 
 
 def test_split_part_layout():

@@ -241,7 +241,8 @@ def test_backward_runs_unsplit_in_a_base_size_workspace():
     B, K, G, T, H = 1, 2, 4, 640, 128
     q, k, v, o, lse, dO = _bwd_inputs(B, K, G, T, H, seed=29)
     up = lambda n: (n + 255) // 256 * 256
-    base = up(B * K * G * T * 4) + up(B * (T // (128 // G) + -(-T // 64)) * 8)
+    # D rows, the per-tile segment ranges, one segment-run byte per 64-key tile
+    base = up(B * K * G * T * 4) + up(B * (T // (128 // G) + -(-T // 64)) * 8) + up(B * -(-T // 64))
     assert binding.fa_bwd_workspace_size(B, K, G, T, T, H) > base   # the split part exists here
     dev = q.device
     outs = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
