@@ -99,6 +99,21 @@ bool make_kv_map(CUtensorMap* m, const void* ptr, int BK, int S, int H, int rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// k-like tensor [B*K, S, H] viewed as 4-D {64 dims, S, H/64 chunks, B*K} with
+// a box of `rows` keys x `chunks` x 64 dims: one copy lands `chunks`
+// consecutive [rows x 128 B] swizzled chunks, the layout per-chunk boxes give.
+bool make_kv_tile_map(CUtensorMap* m, const void* ptr, int BK, int S, int H, int rows, int chunks) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)S, (cuuint64_t)(H / 64), (cuuint64_t)BK};
+  cuuint64_t strides[3] = {(cuuint64_t)H * 2, 128, (cuuint64_t)S * H * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)rows, (cuuint32_t)chunks, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Shared shape checks of the forward and backward passes.
 int check_shapes(int B, int K, int G, int T, int S, int H, int causal, const void* seg_q,
                  const void* seg_kv) {
@@ -171,8 +186,9 @@ int fwd_common(const void* q, const void* k, const void* v, const int32_t* seg_q
   }
   fa::FwdArgs a{};
   const int BK = B * K;
-  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_map(&a.tm_k, k, BK, S, H, fa::kKvRows) ||
-      !make_kv_map(&a.tm_v, v, BK, S, H, fa::kKvRows) || !make_q_map(&a.tm_o, o, BK, G, T, H))
+  const int cc = fa::fwd_copy_chunks(H);
+  if (!make_q_map(&a.tm_q, q, BK, G, T, H) || !make_kv_tile_map(&a.tm_k, k, BK, S, H, fa::kKvRows, cc) ||
+      !make_kv_tile_map(&a.tm_v, v, BK, S, H, fa::kKvRows, cc) || !make_q_map(&a.tm_o, o, BK, G, T, H))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;

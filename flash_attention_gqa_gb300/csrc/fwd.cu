@@ -18,7 +18,8 @@
 // first 64 columns of its S buffer and is the A operand of O += P V.
 //
 // Shared memory: Q tile (H/64 chunks of [128 rows x 128 B]), a ring of
-// kSlots chunks of [128 keys x 64 dims] bf16 fed by TMA with 128-byte swizzle,
+// kSlots chunks of [128 keys x 64 dims] bf16 fed by TMA with 128-byte swizzle
+// (one copy per fwd_copy_chunks(H) consecutive chunks of a K or V tile),
 // the per-tile schedule and the mbarriers.
 #include <cuda_bf16.h>
 #include "block_mask.cuh"
@@ -251,6 +252,7 @@ template <int H>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdSmem<H>;
   constexpr int HC = L::HC;
+  constexpr int CC = fwd_copy_chunks(H);  // chunks per K/V copy
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
@@ -409,21 +411,24 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         else { is_k = false; n = u / 2 - 1; }
         const int j = sched[n] & 0x7fff;
         const CUtensorMap* m = is_k ? &a.tm_k : &a.tm_v;
-        for (int c = 0; c < HC; ++c, ++seq) {
-          const int slot = seq % kSlots;
-          if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
-            ok = false;
-            break;
+        // The unit's HC chunks sit in consecutive slots (kSlots is a multiple
+        // of HC).  Each copy fills CC of them and completes on the first one's
+        // barrier, once every chunk's previous reader has released its slot.
+        for (int cc = 0; cc < HC && ok; cc += CC, seq += CC) {
+          for (int c = 0; c < CC && ok; ++c) {
+            const uint32_t sq = seq + c;
+            if (sq >= kSlots && !mbar_wait(bars.empty(sq % kSlots), ((sq / kSlots) - 1) & 1, ab)) ok = false;
           }
-          mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
-          tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
-                      j * kKvRows, bk);
+          if (!ok) break;
+          const int slot = seq % kSlots;
+          mbar_arrive_expect_tx(bars.full(slot), CC * kChunkBytes);
+          tma_load_4d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), 0, j * kKvRows, cc, bk);
         }
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
         const uint32_t first = seq > kSlots ? seq - kSlots : 0;
-        for (uint32_t s = first; s < seq; ++s)
+        for (uint32_t s = first; s < seq; s += CC)  // one copy per CC chunks, on its first slot
           mbar_wait_teardown(bars.full(s % kSlots), (s / kSlots) & 1, a.wait_limit_ns);
       }
     }
@@ -441,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!mbar_wait(bars.p_full(n & 1), (n >> 1) & 1, ab)) return false;
         const uint32_t seq0 = unit_v(n, n_tiles) * HC;
         const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
-        for (int c = 0; c < HC; ++c)
-          if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) return false;
+        for (int c = 0; c < HC; c += CC)  // every copy of the V tile
+          if (!mbar_wait(bars.full(slot0 + c), (seq0 / kSlots) & 1, ab)) return false;
         tc_fence_after();
         const uint32_t p_col = 256 + 128 * (n & 1);
         const uint64_t bv = sdesc_add(dv0, slot0 * kChunkBytes);
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const uint32_t seq0 = unit_k(n) * HC;
         const int slot0 = seq0 % kSlots;
         for (int c = 0; c < HC && ok; ++c) {
-          if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(bars.full(slot0 + c - c % CC), (seq0 / kSlots) & 1, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t a = sdesc_add(dq0, c * kChunkBytes);
           const uint64_t bk_ = sdesc_add(dk0, (slot0 + c) * kChunkBytes);
@@ -597,6 +602,7 @@ template <int H>
 __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const __grid_constant__ FwdArgs a) {
   using L = PFwdSmem<H>;
   constexpr int HC = L::HC;
+  constexpr int CC = fwd_copy_chunks(H);  // chunks per K/V copy
   static_assert(H <= 128, "two O accumulators must fit next to the S buffers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -790,22 +796,25 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           else { is_k = false; n = u / 2 - 1; }
           const int j = list[n] & 0x7fff;
           const CUtensorMap* m = is_k ? &a.tm_k : &a.tm_v;
-          for (int c = 0; c < HC; ++c, ++seq) {
-            const int slot = seq % kSlots;
-            if (seq >= kSlots && !mbar_wait(bars.empty(slot), ((seq / kSlots) - 1) & 1, ab)) {
-              ok = false;
-              break;
+          // The unit's HC chunks sit in consecutive slots (kSlots is a multiple
+          // of HC).  Each copy fills CC of them and completes on the first one's
+          // barrier, once every chunk's previous reader has released its slot.
+          for (int cc = 0; cc < HC && ok; cc += CC, seq += CC) {
+            for (int c = 0; c < CC && ok; ++c) {
+              const uint32_t sq = seq + c;
+              if (sq >= kSlots && !mbar_wait(bars.empty(sq % kSlots), ((sq / kSlots) - 1) & 1, ab)) ok = false;
             }
-            mbar_arrive_expect_tx(bars.full(slot), kChunkBytes);
-            tma_load_3d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), c * 64,
-                        j * kKvRows, bk);
+            if (!ok) break;
+            const int slot = seq % kSlots;
+            mbar_arrive_expect_tx(bars.full(slot), CC * kChunkBytes);
+            tma_load_4d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), 0, j * kKvRows, cc, bk);
           }
         }
         if (ok) mbar_arrive(item_free(b));  // done with this item's schedule
       }
       if (!ok) {
         const uint32_t first = seq > kSlots ? seq - kSlots : 0;
-        for (uint32_t q = first; q < seq; ++q)
+        for (uint32_t q = first; q < seq; q += CC)  // one copy per CC chunks, on its first slot
           mbar_wait_teardown(bars.full(q % kSlots), (q / kSlots) & 1, a.wait_limit_ns);
       }
     }
@@ -836,7 +845,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           const uint32_t seq0 = seq_base + unit_k(n) * HC;
           const int slot0 = seq0 % kSlots;
           for (int c = 0; c < HC && ok; ++c) {
-            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) { ok = false; break; }
+            if (!mbar_wait(bars.full(slot0 + c - c % CC), (seq0 / kSlots) & 1, ab)) { ok = false; break; }
             tc_fence_after();
             const uint64_t qa = sdesc_add(dq0, c * kChunkBytes);
             const uint64_t kb = sdesc_add(dk0, (slot0 + c) * kChunkBytes);
@@ -877,8 +886,8 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           if (!mbar_wait(bars.p_full(Nn & 1), (Nn >> 1) & 1, ab)) { ok = false; break; }
           const uint32_t seq0 = seq_base + unit_v(n, n_tiles) * HC;
           const int slot0 = seq0 % kSlots;  // the unit's HC chunks sit in consecutive slots
-          for (int c = 0; c < HC && ok; ++c)
-            if (!mbar_wait(bars.full(slot0 + c), ((seq0 + c) / kSlots) & 1, ab)) ok = false;
+          for (int c = 0; c < HC && ok; c += CC)  // every copy of the V tile
+            if (!mbar_wait(bars.full(slot0 + c), (seq0 / kSlots) & 1, ab)) ok = false;
           if (!ok) break;
           tc_fence_after();
           const uint32_t p_col = 256 + 128 * (Nn & 1);
@@ -900,18 +909,62 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
     }
   } else {
     // --------------------------------------------------- softmax, epilogue
+    // The epilogue of item k runs after the first softmax tile of item k + 1,
+    // so the tensor core has that tile's products to work on meanwhile (O is
+    // double buffered per item).  Thread 0 awaits the read of a TMA store one
+    // tile later, before it frees the item's buffers.
     const int r = tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int g = r / Tb;
     bool ok = true;
     int N = 0;
+    // the item whose epilogue is pending
+    bool pend = false;
+    int p_k = 0, p_tiles = 0, p_last = 0, p_t0 = 0, p_bk = 0;
+    float p_m = -INFINITY, p_l = 0.f;
+    int free_b = -1;  // thread 0: buffers whose O store still reads shared memory
+    auto release = [&]() {
+      if (tid == 0 && free_b >= 0) {
+        bulk_wait_read0();
+        mbar_arrive(item_free(free_b));  // Q[b] (staging) and O[b] may be reused
+        free_b = -1;
+      }
+    };
+    auto finish = [&]() -> bool {
+      pend = false;
+      const int b = p_k & 1;
+      const bool have = p_tiles > 0 && warp_wait(bars.pv_done(p_last & 1), (p_last >> 1) & 1, ab);
+      if (p_tiles > 0 && !have) return false;
+      if (have) tc_fence_after();
+      const float inv = (have && p_l > 0.f) ? 1.f / p_l : 0.f;
+      const float lse_row = (have && p_l > 0.f) ? (p_m + __log2f(p_l)) * kLn2 : -INFINITY;
+      // Q[b] is free: every product of the item has completed (pv_done of its
+      // last tile follows them all), or there were none.
+      stage_o_row<H>(sm + q_tile(b), tmem, lane_base, 128u * b, r, have, inv);
+      const int t = p_t0 + (r - g * Tb);
+      if (t < a.T) a.lse[((long)p_bk * a.G + g) * a.T + t] = lse_row;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(o_staged);
+      if (tid == 0) {
+        release();
+        if (!mbar_wait(o_staged, p_k & 1, ab)) return false;
+        for (int c = 0; c < HC; ++c)
+          tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, p_t0, 0, p_bk);
+        bulk_commit();
+        free_b = b;
+      }
+      return true;
+    };
     for (int k = 0; ok; ++k) {
       const int b = k & 1;
+      release();  // the scheduler waits for it before it refills buffers b
       if (!warp_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
       volatile int* info = info_all + 4 * b;
       const int n_tiles = info[0];
       if (n_tiles < 0) break;
       const int qt = info[1], bk = info[2], bb = bk / a.K;
-      const int t0 = qt * Tb, g = r / Tb, t = t0 + (r - g * Tb);
+      const int t0 = qt * Tb, t = t0 + (r - g * Tb);
       const bool valid = t < a.T;
       const int my_seg = (segs && valid) ? a.seg_q[(long)bb * a.T + t] : 0;
       const uint16_t* list = sched(b);
@@ -923,31 +976,21 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
           ok = false;
           break;
         }
+        if (n == 0 && pend) {
+          if (!finish()) { ok = false; break; }
+        } else {
+          release();
+        }
       }
       if (!ok) break;
-      const int last = N + n_tiles - 1;
-      const bool have = n_tiles > 0 && warp_wait(bars.pv_done(last & 1), (last >> 1) & 1, ab);
-      if (n_tiles > 0 && !have) { ok = false; break; }
-      if (have) tc_fence_after();
-      const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
-      const float lse_row = (have && l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      // Q[b] is free: every product of this item has completed (pv_done of its
-      // last tile follows them all), or there were none.
-      stage_o_row<H>(sm + q_tile(b), tmem, lane_base, o_col, r, have, inv);
-      if (valid) a.lse[((long)bk * a.G + g) * a.T + t] = lse_row;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(o_staged);
-      if (tid == 0) {
-        if (!mbar_wait(o_staged, k & 1, ab)) { ok = false; break; }
-        for (int c = 0; c < HC; ++c)
-          tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, t0, 0, bk);
-        bulk_commit();
-        bulk_wait_read0();
-        mbar_arrive(item_free(b));  // Q[b] (staging) and O[b] may be reused
-      }
+      if (pend && !finish()) { ok = false; break; }  // an item without tiles
+      pend = true;
+      p_k = k; p_tiles = n_tiles; p_last = N + n_tiles - 1; p_t0 = t0; p_bk = bk;
+      p_m = m_ref; p_l = l;
       N += n_tiles;
     }
+    if (ok && pend) ok = finish();
+    release();
   }
 
   tc_fence_before();

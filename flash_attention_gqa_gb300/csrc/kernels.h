@@ -9,6 +9,10 @@ namespace fa {
 // Tile geometry shared by every kernel.
 constexpr int kRows = 128;     // packed query rows per Q tile (G heads x 128/G positions)
 constexpr int kKvRows = 128;   // key/value rows per KV tile in the forward
+// 64-dim chunks the forward moves per K or V copy: the whole tile up to
+// H = 128; at H = 256 one chunk, so the first products of a K tile can start
+// while its other chunks are still landing.
+constexpr int fwd_copy_chunks(int H) { return H >= 256 ? 1 : H / 64; }
 constexpr int kMaxKvTiles = 1024;  // S <= 131072
 
 // Segment-id layout of a KV tile, one byte per tile: the index of the key
@@ -28,7 +32,7 @@ struct BlockMask {
 
 struct FwdArgs {
   CUtensorMap tm_q;   // q as 4-D {H, T, G, B*K}, box {64, 128/G, G, 1}, 128B swizzle
-  CUtensorMap tm_k;   // k as 3-D {H, S, B*K},   box {64, 128, 1}
+  CUtensorMap tm_k;   // k as 4-D {64, S, H/64, B*K}, box {64, 128, fwd_copy_chunks(H), 1}
   CUtensorMap tm_v;   // v, same as k
   CUtensorMap tm_o;   // o, same geometry as q (TMA store of the finished tile)
   void* o;            // bf16 [B*K, G, T, H]
