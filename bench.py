@@ -47,12 +47,12 @@ _CAPTURE = ("one --metrics capture on one GB300 (medians of 15 launches; profile
             "box to box with L2 residency")
 NCU_TRAFFIC: dict = {
     "gqa_causal_h256_t8192": {
-        "fa_fwd_kernel<256>": {"bytes_per_launch": 108218000, "src": "fwd.cu",
-                               "src_sha": "d2b8009a8cd7663c", "note": _CAPTURE},
-        "fa_bwd_dkdv1_kernel<256, 64, 0>": {"bytes_per_launch": 193545000, "src": "bwd.cu",
-                                            "src_sha": "c3691a3bf755d84d", "note": _CAPTURE},
-        "fa_bwd_dq_kernel<256, 64>": {"bytes_per_launch": 188660000, "src": "bwd.cu",
-                                      "src_sha": "c3691a3bf755d84d", "note": _CAPTURE},
+        "fa_fwd_kernel<256>": {"bytes_per_launch": 108094000, "src": "fwd.cu",
+                               "src_sha": "ccc06d0b515abce1", "note": _CAPTURE},
+        "fa_bwd_dkdv1_kernel<256, 64, 0, 0>": {"bytes_per_launch": 193123000, "src": "bwd.cu",
+                                               "src_sha": "dcda10fcedc593e6", "note": _CAPTURE},
+        "fa_bwd_dq_kernel<256, 64, 0>": {"bytes_per_launch": 188404000, "src": "bwd.cu",
+                                         "src_sha": "dcda10fcedc593e6", "note": _CAPTURE},
     },
 }
 
@@ -77,10 +77,10 @@ def kernel_names(w: inputs.Workload, n_splits: int, masked: bool) -> dict:
         rc, kvr, qs = binding.fa_bwd_plan(w.B, w.K, w.G, w.T, w.S, w.H, w.causal,
                                           masked or w.segments, sms)
         assert rc == binding.FA_OK, binding.status_string(rc)
-        split = int(qs > 1)
-        dkdv = (f"fa_bwd_dkdv1_kernel<256, {kvr}, {split}>" if w.H == 256
-                else f"fa_bwd_dkdv_kernel<{max(w.H, 128)}, {kvr}, {split}>")
-        dq = f"fa_bwd_dq_kernel<{max(w.H, 128)}, {kvr}>"
+        split, segs = int(qs > 1), int(w.segments)
+        dkdv = (f"fa_bwd_dkdv1_kernel<256, {kvr}, {split}, {segs}>" if w.H == 256
+                else f"fa_bwd_dkdv_kernel<{max(w.H, 128)}, {kvr}, {split}, {segs}>")
+        dq = f"fa_bwd_dq_kernel<{max(w.H, 128)}, {kvr}, {segs}>"
         pre = f"bwd_preprocess_kernel<{w.H}>" + (" + seg_ranges_kernel x2" if w.segments else "")
         names.update(pre=pre, dkdv=dkdv, dq=dq, bwd=f"fa_bwd_masked: {pre} + {dkdv} + {dq}")
     return names
