@@ -580,21 +580,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 // 64 on the tensor pipe), so each product type has its own issuing warp.
 // Tensor memory: O[b] at columns [128 b, 128 b + H), S buffers at 256 and 384.
 constexpr int kPThreads = 256;
+constexpr int kSchedBufs = 4;  // KV-tile schedules in flight (items)
 
 template <int H>
 struct PFwdSmem {
   static constexpr int HC = H / 64;
   static constexpr uint32_t q_off = 0;  // Q[b] at q_off + b * HC * kChunkBytes
   static constexpr uint32_t ring_off = 2 * HC * kChunkBytes;
-  static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[2][kMaxKvTiles]
-  static constexpr uint32_t runs_off = sched_off + 2 * kMaxKvTiles * 2;   // uint8[2][kMaxKvTiles]
-  static constexpr uint32_t bar_off = runs_off + 2 * kMaxKvTiles;
-  // q_full[2], sched_full[2], item_free[2], then the Bars block (full, empty,
-  // s_full, p_full, pv_done, teardown), the O += P V issuer's teardown, and
-  // o_staged
-  static constexpr int n_bars = 6 + 1 + 2 * kSlots + 7 + 1 + 1;
-  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, item info[2][4]
-  static constexpr uint32_t bytes = misc_off + 64;
+  static constexpr uint32_t sched_off = ring_off + kSlots * kChunkBytes;  // uint16[kSchedBufs][kMaxKvTiles]
+  static constexpr uint32_t runs_off = sched_off + kSchedBufs * kMaxKvTiles * 2;  // uint8[kSchedBufs][kMaxKvTiles]
+  static constexpr uint32_t bar_off = runs_off + kSchedBufs * kMaxKvTiles;
+  // q_full[2], item_free[2], sched_full[kSchedBufs], list_free[kSchedBufs], then
+  // the Bars block (full, empty, s_full, p_full, pv_done, teardown), the
+  // O += P V issuer's teardown, and o_staged
+  static constexpr int n_head = 4 + 2 * kSchedBufs;
+  static constexpr int n_bars = n_head + 1 + 2 * kSlots + 7 + 1 + 1;
+  static constexpr uint32_t misc_off = bar_off + n_bars * 8;  // tmem slot, abort, item info[kSchedBufs][4]
+  static constexpr uint32_t bytes = misc_off + 16 + kSchedBufs * 16;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
@@ -609,22 +611,26 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
   uint8_t* sm = smem_raw + (((raw + 1023) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t pb = sbase + L::bar_off;
+  // Q[b] and O[b] are double buffered by item (b = k & 1); the KV-tile
+  // schedule of item k sits in list buffer k % kSchedBufs, so the scheduler
+  // classifies up to kSchedBufs - 2 items ahead of the Q buffers' release.
   auto q_full = [&](int b) { return pb + 8 * b; };
-  auto sched_full = [&](int b) { return pb + 8 * (2 + b); };
-  auto item_free = [&](int b) { return pb + 8 * (4 + b); };
-  Bars bars{pb + 8 * 6};
-  const uint32_t teardown_pv = pb + 8 * (6 + 1 + 2 * kSlots + 7);
+  auto item_free = [&](int b) { return pb + 8 * (2 + b); };
+  auto sched_full = [&](int sb) { return pb + 8 * (4 + sb); };
+  auto list_free = [&](int sb) { return pb + 8 * (4 + kSchedBufs + sb); };
+  Bars bars{pb + 8 * L::n_head};
+  const uint32_t teardown_pv = pb + 8 * (L::n_head + 1 + 2 * kSlots + 7);
   // every softmax thread has staged its row of O / l: the storing thread waits
   // on it with a bound (a named barrier could not give up if a warp aborted
   // before reaching it)
-  const uint32_t o_staged = pb + 8 * (6 + 1 + 2 * kSlots + 7 + 1);
+  const uint32_t o_staged = pb + 8 * (L::n_head + 1 + 2 * kSlots + 7 + 1);
   auto sched = [&](int b) { return reinterpret_cast<uint16_t*>(sm + L::sched_off) + b * kMaxKvTiles; };
   // segment-run byte of each schedule entry (segment ids only)
   auto runs_of = [&](int b) { return sm + L::runs_off + b * kMaxKvTiles; };
   auto q_tile = [&](int b) { return L::q_off + (uint32_t)b * HC * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::misc_off + 4);
-  volatile int* info_all = reinterpret_cast<volatile int*>(sm + L::misc_off + 16);  // [2][4]
+  volatile int* info_all = reinterpret_cast<volatile int*>(sm + L::misc_off + 16);  // [kSchedBufs][4]
   const Abort ab{abort_flag, a.wait_limit_ns, a.err};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -639,10 +645,14 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
     *abort_flag = 0;
     for (int b = 0; b < 2; ++b) {
       mbar_init(q_full(b), 1);
-      mbar_init(sched_full(b), 1);
-      // producer done with the schedule, both MMA warps have read the tile
-      // count, epilogue stored: the item's buffers may be refilled
+      // producer done with the item, both MMA warps have read the tile count,
+      // epilogue stored: Q[b] and O[b] may be refilled
       mbar_init(item_free(b), 4);
+    }
+    for (int sb = 0; sb < kSchedBufs; ++sb) {
+      mbar_init(sched_full(sb), 1);
+      // the producer and the four softmax warps have read the item's list
+      mbar_init(list_free(sb), 5);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(bars.full(s), 1);
@@ -671,16 +681,16 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
     bool ok = true;
     int k = 0;
     for (;; ++k) {
-      const int b = k & 1;
-      // buffers b were last used by item k - 2
-      if (k >= 2 && !warp_wait(item_free(b), ((k >> 1) - 1) & 1, ab)) { ok = false; break; }
-      volatile int* info = info_all + 4 * b;
+      const int b = k & 1, sb = k % kSchedBufs;
+      // list buffer sb was last read by item k - kSchedBufs
+      if (k >= kSchedBufs && !warp_wait(list_free(sb), ((k / kSchedBufs) - 1) & 1, ab)) { ok = false; break; }
+      volatile int* info = info_all + 4 * sb;
       // Snake order over the LPT list: even rounds left to right, odd rounds
       // right to left, so every CTA's share of the decreasing sizes evens out.
       const int G = (int)gridDim.x;
       const int item = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
       if (item >= n_items) {
-        if (lane == 0) { info[0] = -1; mbar_arrive(sched_full(b)); }
+        if (lane == 0) { info[0] = -1; mbar_arrive(sched_full(sb)); }
         break;
       }
       const int qt = a.n_qtiles - 1 - item / BKn, bk = item % BKn, bb = bk / a.K;
@@ -702,7 +712,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       }
       // Classify 32 KV tiles at a time, one per lane, and compact the
       // non-empty ones (ballot prefix sums) into the schedule.
-      uint16_t* list = sched(b);
+      uint16_t* list = sched(sb);
       int count = 0;
       for (int j0 = 0; j0 < n_kv; j0 += 32) {
         const int j = j0 + lane;
@@ -750,11 +760,13 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
         if (c != TILE_EMPTY) {
           const int at = count + __popc(m & ((1u << lane) - 1));
           list[at] = (uint16_t)(j | (c == TILE_PARTIAL ? 0x8000 : 0));
-          runs_of(b)[at] = run;
+          runs_of(sb)[at] = run;
         }
         count += __popc(m);
       }
       __syncwarp();
+      // Q[b] and O[b] were last used by item k - 2
+      if (k >= 2 && !warp_wait(item_free(b), ((k >> 1) - 1) & 1, ab)) { ok = false; break; }
       if (lane == 0) {
         info[0] = count; info[1] = qt; info[2] = bk;
         if (count > 0) {
@@ -764,7 +776,7 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
         } else {
           mbar_arrive(q_full(b));  // keep the phase count of q_full(b) in step
         }
-        mbar_arrive(sched_full(b));
+        mbar_arrive(sched_full(sb));
       }
     }
     // Q copies still in flight (the last two items) land before the CTA exits.
@@ -779,13 +791,13 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       uint32_t seq = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int b = k & 1;
-        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
-        volatile int* info = info_all + 4 * b;
+        const int b = k & 1, sb = k % kSchedBufs;
+        if (!mbar_wait(sched_full(sb), (k / kSchedBufs) & 1, ab)) { ok = false; break; }
+        volatile int* info = info_all + 4 * sb;
         const int n_tiles = info[0];
         if (n_tiles < 0) break;
         const int bk = info[2];
-        const uint16_t* list = sched(b);
+        const uint16_t* list = sched(sb);
         for (int u = 0; u < 2 * n_tiles && ok; ++u) {
           // unit 0: K(0); last unit: V(N-1); odd u: K((u+1)/2); even u: V(u/2 - 1)
           bool is_k;
@@ -810,7 +822,10 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
             tma_load_4d(sbase + L::ring_off + slot * kChunkBytes, m, bars.full(slot), 0, j * kKvRows, cc, bk);
           }
         }
-        if (ok) mbar_arrive(item_free(b));  // done with this item's schedule
+        if (ok) {  // done with this item's schedule
+          mbar_arrive(list_free(sb));
+          mbar_arrive(item_free(b));
+        }
       }
       if (!ok) {
         const uint32_t first = seq > kSlots ? seq - kSlots : 0;
@@ -827,9 +842,9 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       uint32_t seq_base = 0;  // ring chunks of earlier items
       int N = 0;              // tiles of earlier items (S / P buffer and parity counter)
       for (int k = 0; ok; ++k) {
-        const int b = k & 1;
-        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
-        const int n_tiles = info_all[4 * b];
+        const int b = k & 1, sb = k % kSchedBufs;
+        if (!mbar_wait(sched_full(sb), (k / kSchedBufs) & 1, ab)) { ok = false; break; }
+        const int n_tiles = info_all[4 * sb];
         if (n_tiles < 0) break;
         // Nothing else of the item's shared state is read here (Q[b] is
         // released by the epilogue, which waits for every product of the item).
@@ -875,12 +890,12 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       uint32_t seq_base = 0;
       int N = 0;
       for (int k = 0; ok; ++k) {
-        const int b = k & 1;
-        if (!mbar_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
-        const int n_tiles = info_all[4 * b];
+        const int b = k & 1, sb = k % kSchedBufs;
+        if (!mbar_wait(sched_full(sb), (k / kSchedBufs) & 1, ab)) { ok = false; break; }
+        const int n_tiles = info_all[4 * sb];
         if (n_tiles < 0) break;
         mbar_arrive(item_free(b));
-        const uint32_t o_col = 128u * b;  // free: sched_full(b) follows item k-2's epilogue
+        const uint32_t o_col = 128u * b;  // free: sched_full follows item k-2's release of O[b]
         for (int n = 0; n < n_tiles && ok; ++n) {
           const int Nn = N + n;
           if (!mbar_wait(bars.p_full(Nn & 1), (Nn >> 1) & 1, ab)) { ok = false; break; }
@@ -946,32 +961,39 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(o_staged);
-      if (tid == 0) {
-        release();
-        if (!mbar_wait(o_staged, p_k & 1, ab)) return false;
-        for (int c = 0; c < HC; ++c)
-          tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, p_t0, 0, p_bk);
-        bulk_commit();
-        free_b = b;
+      bool stored = true;
+      if (warp == 0) {  // the outcome of thread 0's wait is the whole warp's
+        if (lane == 0) {
+          release();
+          stored = mbar_wait(o_staged, p_k & 1, ab);
+          if (stored) {
+            for (int c = 0; c < HC; ++c)
+              tma_store_4d(&a.tm_o, sbase + q_tile(b) + c * kChunkBytes, c * 64, p_t0, 0, p_bk);
+            bulk_commit();
+            free_b = b;
+          }
+        }
+        stored = __shfl_sync(0xffffffffu, stored, 0);
       }
-      return true;
+      return stored;
     };
     for (int k = 0; ok; ++k) {
-      const int b = k & 1;
+      const int b = k & 1, sb = k % kSchedBufs;
       release();  // the scheduler waits for it before it refills buffers b
-      if (!warp_wait(sched_full(b), (k >> 1) & 1, ab)) { ok = false; break; }
-      volatile int* info = info_all + 4 * b;
+      if (!warp_wait(sched_full(sb), (k / kSchedBufs) & 1, ab)) { ok = false; break; }
+      volatile int* info = info_all + 4 * sb;
       const int n_tiles = info[0];
       if (n_tiles < 0) break;
       const int qt = info[1], bk = info[2], bb = bk / a.K;
       const int t0 = qt * Tb, t = t0 + (r - g * Tb);
       const bool valid = t < a.T;
       const int my_seg = (segs && valid) ? a.seg_q[(long)bb * a.T + t] : 0;
-      const uint16_t* list = sched(b);
+      const uint16_t* list = sched(sb);
+      const uint8_t* runs = runs_of(sb);
       const uint32_t o_col = 128u * b;
       float m_ref = -INFINITY, l = 0.f;
       for (int n = 0; n < n_tiles; ++n) {
-        if (!softmax_tile<H>(a, tmem, lane_base, list[n], runs_of(b)[n], n, N + n, t, g, valid, my_seg, bb,
+        if (!softmax_tile<H>(a, tmem, lane_base, list[n], runs[n], n, N + n, t, g, valid, my_seg, bb,
                              bk % a.K, bars, ab, m_ref, l, o_col)) {
           ok = false;
           break;
@@ -983,6 +1005,8 @@ __global__ void __launch_bounds__(kPThreads, 1) fa_fwd_persistent_kernel(const _
         }
       }
       if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(list_free(sb));  // this warp has read the item's list
       if (pend && !finish()) { ok = false; break; }  // an item without tiles
       pend = true;
       p_k = k; p_tiles = n_tiles; p_last = N + n_tiles - 1; p_t0 = t0; p_bk = bk;
