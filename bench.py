@@ -47,11 +47,11 @@ _CAPTURE = ("one --metrics capture on one GB300 (medians of 15 launches; profile
             "box to box with L2 residency")
 NCU_TRAFFIC: dict = {
     "gqa_causal_h256_t8192": {
-        "fa_fwd_kernel<256>": {"bytes_per_launch": 108094000, "src": "fwd.cu",
-                               "src_sha": "ccc06d0b515abce1", "note": _CAPTURE},
-        "fa_bwd_dkdv1_kernel<256, 64, 0, 0>": {"bytes_per_launch": 193123000, "src": "bwd.cu",
+        "fa_fwd_kernel<256>": {"bytes_per_launch": 108200000, "src": "fwd.cu",
+                               "src_sha": "083071e8dc022dc9", "note": _CAPTURE},
+        "fa_bwd_dkdv1_kernel<256, 64, 0, 0>": {"bytes_per_launch": 170500000, "src": "bwd.cu",
                                                "src_sha": "dcda10fcedc593e6", "note": _CAPTURE},
-        "fa_bwd_dq_kernel<256, 64, 0>": {"bytes_per_launch": 188404000, "src": "bwd.cu",
+        "fa_bwd_dq_kernel<256, 64, 0>": {"bytes_per_launch": 188400000, "src": "bwd.cu",
                                          "src_sha": "dcda10fcedc593e6", "note": _CAPTURE},
     },
 }
