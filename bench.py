@@ -54,6 +54,13 @@ NCU_TRAFFIC: dict = {
         "fa_bwd_dq_kernel<256, 64, 0>": {"bytes_per_launch": 188400000, "src": "bwd.cu",
                                          "src_sha": "dcda10fcedc593e6", "note": _CAPTURE},
     },
+    "gqa_packed_docs_h128_t4096": {
+        "fa_bwd_dkdv_kernel<128, 128, 0, 1>": {
+            "bytes_per_launch": 426100000, "src": "bwd.cu", "src_sha": "dcda10fcedc593e6",
+            "note": ("one ncu --set full capture of one launch on one GB300 "
+                     "(profiles/full_packed_docs_h128_t4096.md); DRAM traffic of the same code "
+                     "varies box to box with L2 residency")},
+    },
 }
 
 
