@@ -51,9 +51,17 @@ def full_unit(job: dict) -> dict:
     dq, dk and dv (job["part"] == "bwd").
 
     Inputs are the unit's slices as [1, 1, G, T, H] / [1, 1, S, H] float32
-    arrays (bf16 values, exact) and [1, T] / [1, S] segment ids."""
+    arrays (bf16 values, exact) and [1, T] / [1, S] segment ids; job["window"]
+    (T, S, window), if given, adds a causal sliding-window mask."""
     import oracle
     kw = dict(causal=job["causal"], seg_q=job["seg_q"], seg_kv=job["seg_kv"], row_block=256)
+    if job.get("window"):
+        # causal sliding window t - window < s <= t + (S - T), as a dense [1, T, S]
+        # keep-mask (a layout: which pairs exist)
+        T, S, window = job["window"]
+        t = np.arange(T)[:, None]
+        s = np.arange(S)[None, :]
+        kw["mask"] = ((s <= t + (S - T)) & (s > t + (S - T) - window))[None]
     if job["part"] == "fwd":
         o, lse = oracle.attention_forward(job["q"], job["k"], job["v"], **kw)
         return {"o": err_sums(job["o_gpu"], o), "lse": err_sums(job["lse_gpu"], lse)}

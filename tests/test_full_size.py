@@ -9,6 +9,8 @@ and must give the same bits.
 * causal H=256, T=S=8192 (model_dim 4096, 16 query heads, 2 kv heads) and the
   packed-document workload (causal + segment ids, H=128, T=S=4096): every
   element of O, lse, dq, dk and dv against the full oracle.
+* the 1024-key causal sliding window (H=128, T=S=8192) as a block-sparse mask:
+  every element of O, lse, dq, dk and dv against the oracle's dense mask.
 * causal H=256, T=S=32768: O and lse at one query row of every Q tile of every
   head (the row within the tile rotates from tile to tile), and dk, dv over
   three whole 64-key tiles (the first, one in the middle, the last) of both kv
@@ -94,6 +96,38 @@ def check_every_element(name):
                              dk_gpu=f32(dk[u]), dv_gpu=f32(dv[u])))
     res = pool.run(pool.full_unit, jobs)
     o_res, l_res = assert_results(res)
+    assert o_res["n"] == x.q.numel() and l_res["n"] == lse.numel()
+
+
+def test_window1024_h128_t8192_every_element():
+    """The 1024-key causal sliding window given as a block-sparse mask: fa_fwd_masked
+    and fa_bwd_masked with the block metadata built from the dense mask, as bench.py
+    runs them; every element of O, lse, dq, dk, dv against the oracle's dense mask."""
+    w = inputs.WORKLOADS["gqa_window1024_h128_t8192"]
+    x = inputs.make_workload(w)
+    dev = torch.device("cuda")
+    meta = binding.block_mask_from_dense(inputs.window_mask(w.T, w.S, w.window), device=dev)
+    q, k, v, dO = (t.to(dev) for t in (x.q, x.k, x.v, x.dO))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.K, w.G, w.T), dtype=torch.float32, device=dev)
+    binding.fa_fwd_masked(q, k, v, None, None, w.causal, meta, o, lse)
+    grads = [torch.empty_like(t) for t in (q, k, v)]
+    ws = torch.empty(max(256, binding.fa_bwd_workspace_size(w.B, w.K, w.G, w.T, w.S, w.H)),
+                     dtype=torch.uint8, device=dev)
+    binding.fa_bwd_masked(q, k, v, o, lse, dO, None, None, w.causal, meta, *grads, ws)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    o, lse, (dq, dk, dv) = o.cpu(), lse.cpu(), [t.cpu() for t in grads]
+    jobs = []
+    for b in range(w.B):
+        for kh in range(w.K):
+            u = np.s_[b:b + 1, kh:kh + 1]
+            common = dict(q=f32(x.q[u]), k=f32(x.k[u]), v=f32(x.v[u]), seg_q=None, seg_kv=None,
+                          causal=w.causal, window=(w.T, w.S, w.window))
+            jobs.append(dict(common, part="fwd", o_gpu=f32(o[u]), lse_gpu=lse[u].numpy()))
+            jobs.append(dict(common, part="bwd", dO=f32(x.dO[u]), dq_gpu=f32(dq[u]),
+                             dk_gpu=f32(dk[u]), dv_gpu=f32(dv[u])))
+    o_res, l_res = assert_results(pool.run(pool.full_unit, jobs))
     assert o_res["n"] == x.q.numel() and l_res["n"] == lse.numel()
 
 
