@@ -11,6 +11,7 @@ and must give the same bits.
   element of O, lse, dq, dk and dv against the full oracle.
 * the 1024-key causal sliding window (H=128, T=S=8192) as a block-sparse mask:
   every element of O, lse, dq, dk and dv against the oracle's dense mask.
+* one decode step (T=1, S=32768, split-KV): every element of O and lse.
 * causal H=256, T=S=32768: O and lse at one query row of every Q tile of every
   head (the row within the tile rotates from tile to tile), and dk, dv over
   three whole 64-key tiles (the first, one in the middle, the last) of both kv
@@ -170,3 +171,25 @@ def test_causal_h256_t32768_every_q_tile_and_three_key_tiles():
                          dq_gpu=f32(dq[0, kh][:, t_rows]), dk_gpu=f32(dk[0, kh][s_rows]),
                          dv_gpu=f32(dv[0, kh][s_rows])))
     assert_results(pool.run(pool.keys_unit, jobs))
+
+
+def test_decode_h128_s32768_every_element():
+    """One decode step (T=1) against a 32768-key cache, B=8 K=8 G=8 H=128, through
+    fa_fwd_splitkv with the default split count, as bench.py runs it: every element
+    of O and lse against the full oracle."""
+    w = inputs.WORKLOADS["gqa_decode_h128_s32768"]
+    x = inputs.make_workload(w)
+    dev = torch.device("cuda")
+    o, lse = binding.attention_forward_splitkv(x.q.to(dev), x.k.to(dev), x.v.to(dev),
+                                               causal=w.causal)
+    torch.cuda.synchronize()
+    assert binding.fa_check_status() == binding.FA_OK
+    o, lse = o.cpu(), lse.cpu()
+    jobs = []
+    for b in range(w.B):
+        for kh in range(w.K):
+            u = np.s_[b:b + 1, kh:kh + 1]
+            jobs.append(dict(q=f32(x.q[u]), k=f32(x.k[u]), v=f32(x.v[u]), seg_q=None, seg_kv=None,
+                             causal=w.causal, part="fwd", o_gpu=f32(o[u]), lse_gpu=lse[u].numpy()))
+    o_res, l_res = assert_results(pool.run(pool.full_unit, jobs), grads=())
+    assert o_res["n"] == x.q.numel() and l_res["n"] == lse.numel()
