@@ -569,11 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // Persistent forward for H <= 128 without split-KV.  One CTA per SM walks the
 // LPT-ordered Q tiles (items) blockIdx.x, blockIdx.x + gridDim.x, ...  The Q
-// tile, the KV-tile schedule and the O accumulator of an item are double
-// buffered (b = local item index & 1), so a scheduler warp classifies the KV
-// tiles of item k+1 and starts its Q copy while item k runs, and the MMA warp
-// computes the first S tiles of item k+1 while the softmax warps finish item
-// k's epilogue.  Roles (256 threads): warps 0-3 softmax and epilogue, warp 4
+// tile and the O accumulator of an item are double buffered (b = local item
+// index & 1) and its KV-tile schedule sits in a ring of kSchedBufs lists, so a
+// scheduler warp classifies the KV tiles of items ahead and starts the next Q
+// copy while item k runs, the MMA warps compute the first S tiles of item k+1
+// before item k is done, and the softmax warps run item k's epilogue after the
+// first tile of item k+1.  Roles (256 threads): warps 0-3 softmax and epilogue, warp 4
 // K/V producer, warp 5 S = Q K^T issuer and TMEM owner, warp 6 scheduler,
 // warp 7 O += P V issuer.  One thread issuing both products is the limit at
 // H <= 128 (a trace: ~87 cycles per S product and ~123 per P V product against
